@@ -1,0 +1,412 @@
+"""Benchmark of the fused data-parallel step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--workload NAME]
+
+One step = the whole hot path over one batch of synthetic inputs: n*a bf16 micro-step gradients accumulated,
+reduced in ring order, averaged, unscaled and finite-checked, partitioned Adam on the fp32 shards, and the bf16
+all-gather into the n replicas (dp_step_reduce + dp_step_update, the two kernels of dp_step).  The default
+workload is the GPT-2-small parameter list (123,568,896 params), n=8, a=4, ZeRO-1 even shards, loss scale 2^16.
+
+Multi-GPU (torchrun): the path does not shard across GPUs; every rank runs an independent replica of the
+workload (weak scaling), with a barrier and max-over-ranks timing and no collective in the data path.
+
+Rank 0 prints one JSON line.  --impl reference times the float64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused DP grad-reduce+Adam step: Gparams/s and achieved HBM GB/s vs peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", default="gpt2_small")
+    p.add_argument("--sum", choices=["compensated", "plain"], default="compensated")
+    p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end leg (0: same as --steps, max 20)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=1 << 21, help="elements of the oracle's CPU sample")
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(wl):
+    """Algorithmic bytes per parameter: single-pass minimum B1 = 2na + 24 + 2n; the two-pass design adds the
+    fp32 gbar shard written by the reduce kernel and read back by the update kernel (B2 = B1 + 8)."""
+    b1 = 2 * wl.n * wl.a + 24 + 2 * wl.n
+    return b1, b1 + 8, 2 * wl.n * wl.a + 4, 4 + 24 + 2 * wl.n
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("dp_kernels.cu", "dp_device.cuh"):
+        with open(os.path.join(ROOT, "zero_gradient_sync_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, kernel):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        e = j[workload][kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == 0:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if self.t0 is not None and self.t0 - 0.06 <= ts <= (self.t1 or ts) + 0.06]
+        use = inside if inside else rows
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in use if num(p[1]) is not None]
+        smax = [num(p[2]) for p in use if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in use:
+            for nm, v in zip(names, p[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ----------------------------------------------------------------------------------------------- oracle leg
+
+def oracle_sample(wl, host_grads, master_full, sample):
+    """A bounded sample of the workload for the CPU oracle: its first `sample` parameters with the same n, a,
+    stage and an even layout over the sample."""
+    import numpy as np
+    import synth
+    ps = min(sample, wl.psi)
+    segs = synth.layout_even(ps, wl.n)
+    grads = [np.ascontiguousarray(g[:ps]) for g in host_grads]
+    lens = [ps] * wl.n if wl.stage == 0 else synth.shard_lengths(segs, wl.n)
+    master = [np.zeros(L, np.float32) for L in lens]
+    for g, ln, o, lo in segs:
+        master[o][lo:lo + ln] = master_full[g:g + ln]
+    m = [np.zeros(L, np.float32) for L in lens]
+    v = [np.zeros(L, np.float32) for L in lens]
+    reps = [np.zeros(ps, np.uint16) for _ in range(wl.n)]
+    return ps, segs, grads, master, m, v, reps
+
+
+def run_oracle_steps(wl, sample_data, steps, threads):
+    import oracle
+    ps, segs, grads, master, m, v, reps = sample_data
+    t = 0
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        res = oracle.step(ps, wl.n, wl.a, wl.stage, segs, grads, master, m, v, reps, wl.lr, wl.beta1, wl.beta2,
+                          wl.eps, wl.loss_scale, t, threads=threads)
+        times.append(time.perf_counter() - t0)
+        t = res["t"]
+    return times
+
+
+def host_inputs_small(wl, ps):
+    import numpy as np
+    import synth
+    grads = [synth.grads_bf16(wl, r, k, 0, ps) for r in range(wl.n) for k in range(wl.a)]
+    return grads, synth.master_f32(wl, 0, ps)
+
+
+def reference_main(args, wl):
+    ws, rank, local = dist_env()
+    if ws > 1 and rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    ps = min(args.cpu_sample, wl.psi)
+    grads, mfull = host_inputs_small(wl, ps)
+    data = oracle_sample(wl, grads, mfull, ps)
+    run_oracle_steps(wl, data, max(0, args.warmup), threads)
+    times = run_oracle_steps(wl, data, args.steps, threads)
+    tot = sum(times)
+    per = tot / max(1, len(times))
+    val = ps / per / 1e9
+    sample = "first %d of %d parameters of the workload per step (even layout over the sample), n=%d, a=%d" % (
+        ps, wl.psi, wl.n, wl.a)
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "Gparams/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": config_of(wl, args),
+           "cpu_baseline": {"value": val, "unit": "Gparams/s", "cores": threads, "kind": "oracle", "sample": sample},
+           "e2e": {"value": val, "unit": "Gparams/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def config_of(wl, args):
+    b1, b2, _, _ = step_bytes(wl)
+    return {"workload": wl.description, "psi": wl.psi, "n": wl.n, "a": wl.a, "zero_stage": wl.stage,
+            "layout": wl.layout, "loss_scale": wl.loss_scale, "sum_mode": args.sum, "grad_dtype": "bf16",
+            "state_dtype": "fp32", "bytes_per_param_single_pass": b1, "bytes_per_param_two_pass": b2,
+            "l2": "inputs larger than L2: %.1f GB streamed per step vs 129 MB L2, no flush" % (b2 * wl.psi / 1e9)}
+
+
+# ----------------------------------------------------------------------------------------------- native leg
+
+def native_main(args, wl):
+    import numpy as np
+    import torch
+
+    import synth
+    import zero_gradient_sync_gb300 as dp
+    from synth import device as sd
+    from zero_gradient_sync_gb300.buffers import StepBuffers
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mode = dp.DP_SUM_COMPENSATED if args.sum == "compensated" else dp.DP_SUM_PLAIN
+    segs = synth.layout_of(wl)
+    layout = dp.Layout(wl.stage, wl.n, wl.psi, segs)
+    bufs = StepBuffers(layout, wl.a, dev)
+    A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
+
+    # Inputs: generated on the host into pinned buffers (kept for the end-to-end leg), then copied to HBM.
+    t_gen = time.time()
+    host_grads = []
+    for r in range(wl.n):
+        for k in range(wl.a):
+            h = torch.empty(wl.psi, dtype=torch.int16, pin_memory=True)
+            synth.grads_bf16(wl, r, k, 0, wl.psi, out=h.numpy().view(np.uint16))
+            host_grads.append(h)
+            bufs.grad(r, k).view(torch.int16).copy_(h)
+    sd.fill_master(bufs.master, wl, segs, wl.stage)
+    torch.cuda.synchronize()
+    t_gen = time.time() - t_gen
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        bufs.reduce(A, wl.loss_scale, mode)
+        bufs.update(A)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as tdist
+            tdist.barrier()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    end = torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(("GPU-" + str(uuid)) if uuid is not None else str(torch.cuda.current_device()))
+    clocks.start()
+    time.sleep(0.15)
+    barrier()
+    torch.cuda.synchronize()
+    l0 = dp.dp_kernel_launches()
+    clocks.mark(0)
+    for k in range(K):
+        ev[k][0].record(stream)
+        bufs.reduce(A, wl.loss_scale, mode)
+        ev[k][1].record(stream)
+        bufs.update(A)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(1)
+    barrier()
+    launches = dp.dp_kernel_launches() - l0
+    total_ms = ev[0][0].elapsed_time(end)
+    red_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    upd_ms = [ev[k][1].elapsed_time(ev[k + 1][0] if k + 1 < K else end) for k in range(K)]
+    clk = clocks.stop()
+    skipped, err = bufs.status()
+    if ws > 1:
+        import torch.distributed as tdist
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / K
+    psi_all = wl.psi * ws
+    value = psi_all / (ms * 1e-3) / 1e9
+
+    b1, b2, red_bytes, upd_bytes = step_bytes(wl)
+    peak, peak_kind = measured_peak()
+    red_avg = sum(red_ms) / K
+    upd_avg = sum(upd_ms) / K
+    red_ach = red_bytes * wl.psi / (red_avg * 1e-3) / 1e9
+    upd_ach = upd_bytes * wl.psi / (upd_avg * 1e-3) / 1e9
+    step_gbs = b2 * wl.psi / (ms * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name, "reduce")
+
+    # End to end through the public call with host buffers: the step's gradients copied from pinned host
+    # memory, the step, and the step's status read back, every step.
+    e2e = None
+    if not args.no_e2e:
+        KE = args.e2e_steps or min(K, 20)
+        host_state = torch.empty(dp.STATE_BYTES, dtype=torch.uint8, pin_memory=True)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(KE):
+            for q, h in enumerate(host_grads):
+                bufs.grads[q].view(torch.int16).copy_(h, non_blocking=True)
+            bufs.step(A, wl.loss_scale, mode)
+            host_state.copy_(bufs.state, non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = s0.elapsed_time(s1) / KE
+        if ws > 1:
+            import torch.distributed as tdist
+            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": psi_all / (e_ms * 1e-3) / 1e9, "unit": "Gparams/s",
+               "h2d_bytes_per_step": 2 * wl.n * wl.a * wl.psi, "d2h_bytes_per_step": dp.STATE_BYTES,
+               "ms_per_step": e_ms, "steps": KE}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        ps = min(args.cpu_sample, wl.psi)
+        host_np = [h[:ps].numpy().view(np.uint16) for h in host_grads]
+        data = oracle_sample(wl, host_np, synth.master_f32(wl, 0, ps), ps)
+        run_oracle_steps(wl, data, 1, threads)
+        reps = 1
+        t_one = sum(run_oracle_steps(wl, data, 1, threads))
+        # about 10-30 s of CPU work (thread-seconds), at most ~12 s of wall time
+        target = max(1, min(int(15.0 / max(1e-6, t_one * threads)), int(12.0 / max(1e-6, t_one))))
+        times = run_oracle_steps(wl, data, target, threads)
+        per = sum(times) / len(times)
+        cpu = {"value": ps / per / 1e9, "unit": "Gparams/s", "cores": threads, "kind": "oracle",
+               "sample": "first %d of %d parameters (even layout over the sample), n=%d, a=%d; %d timed steps, "
+                         "%.1f s wall on %d threads" % (ps, wl.psi, wl.n, wl.a, len(times), sum(times), threads)}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "Gparams/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded Philox4x64 N(0, sigma) bf16 gradients, fp32 master; no dataset)",
+            "config": config_of(wl, args),
+            "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak, "hbm_peak_gbs": peak,
+            "hbm_peak_kind": peak_kind,
+            "roofline": {"bound": "hbm", "kernel": "reduce (accumulate + ring reduce-scatter + average + check)",
+                         "achieved": red_ach, "peak": peak, "unit": "GB/s", "frac": red_ach / peak,
+                         "traffic": traffic, "bytes_per_launch": red_bytes * wl.psi, "avg_ms": red_avg,
+                         "peak_kind": peak_kind},
+            "kernels": {"reduce": {"avg_ms": red_avg, "gbs": red_ach, "bytes_per_param": red_bytes},
+                        "update": {"avg_ms": upd_avg, "gbs": upd_ach, "bytes_per_param": upd_bytes}},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+            "status": {"skipped_last_step": skipped, "error": err}, "setup_s": t_gen,
+        }
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    import synth
+    if args.workload not in synth.WORKLOADS:
+        raise SystemExit("unknown workload %s (have %s)" % (args.workload, ", ".join(synth.WORKLOADS)))
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_main(args, wl)
+    return native_main(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

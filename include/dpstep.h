@@ -1,0 +1,280 @@
+/*
+ * dpstep.h -- C ABI of the fused data-parallel step for one GB300 GPU (sm_103a).
+ *
+ * The step of data-parallel training that follows the backward passes:
+ * n replicas ("ranks") each accumulate the gradients of their a micro-steps,
+ * the ranks' sums are reduced in ring reduce-scatter order, averaged over n
+ * and unscaled by the loss scale under a global non-finite check, a
+ * ZeRO-partitioned mixed-precision Adam updates each rank's fp32 shard of
+ * master weights and moments, and the bf16 parameters are all-gathered into
+ * every replica.  All n ranks' buffers live in one GPU's memory.
+ *
+ * Sources of the operations (page title -- section or paragraph):
+ *  - "Distributed Training: Split along the Four Axes of Data, Tensor,
+ *    Pipeline, and State" -- data-parallelism paragraphs: every rank holds a
+ *    replica; all-reduce sums the local gradients; each rank accumulates a
+ *    micro-steps before one all-reduce; gbar = (sum_r g_r) / n;
+ *    B_global = b x n x a; reduction order and precision change gbar.
+ *  - same page -- ZeRO/FSDP paragraphs: ZeRO-1 shards optimizer state,
+ *    ZeRO-2 also gradients, ZeRO-3/FSDP also parameters; reduce-scatter
+ *    leaves each rank its shard's sum, all-gather collects parameters;
+ *    sharding does not change the update.
+ *  - same page -- memory-budget paragraph: mixed precision keeps an fp32
+ *    master copy and Adam's first and second moments per parameter.
+ *  - same page -- checkpoint and evaluation paragraphs: loss scaling is
+ *    training state that must be kept and aligned.
+ *  - "Data vs Tensor vs Pipeline Parallelism: When to Use Each" -- "Data
+ *    parallelism: split the batch": ring all-reduce traffic 2(N-1)/N x the
+ *    gradient bytes, 16 bytes per parameter, ZeRO-3 16 Psi / N and 1.5x
+ *    traffic; "DP gradient sync at scale": 2(N-1) ring steps.
+ *  The pages name Adam but do not print its equations; the library uses
+ *  standard Adam (Kingma & Ba 2015) with bias correction, epsilon added to
+ *  sqrt(vhat), no weight decay.  Loss-scale unscaling and the skipped step
+ *  are not spelled out on the pages either: gbar is multiplied by
+ *  fl32(1 / (n S)) and any non-finite value skips the whole step.
+ *
+ * Conventions of every entry point:
+ *  - "device" pointers point into memory of the current CUDA device; the
+ *    caller allocates and owns every buffer (the library allocates nothing).
+ *  - Arrays of pointers ("float* const* master") are HOST arrays of n (or
+ *    n*a) DEVICE pointers; the host array is read during the call only.
+ *  - Every device base pointer must be 16-byte aligned (DP_ERR_ALIGNMENT);
+ *    element offsets inside buffers need no alignment.
+ *  - bf16 values are passed as uint16_t bit patterns.
+ *  - Calls are asynchronous on the caller's stream (NULL = legacy default
+ *    stream) and make no host synchronisation, except dp_read_status and
+ *    dp_state_init's implicit none.  A call that returns an error launched
+ *    nothing.  The launch sequence of a step makes no allocation and no
+ *    host synchronisation.
+ *  - A skipped step is not an error: it is reported on the device in
+ *    dp_step_state_t.found_inf and read with dp_read_status.
+ *  - Calls on one dp_step_state_t must be ordered (one stream, or events).
+ */
+#ifndef DPSTEP_H
+#define DPSTEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* dp_stream_t;
+
+typedef enum {
+  DP_OK = 0,
+  DP_ERR_INVALID_ARG = 1, /* bad size, layout, pointer or scalar; nothing launched */
+  DP_ERR_ALIGNMENT = 2,   /* a device base pointer is not 16-byte aligned; nothing launched */
+  DP_ERR_CUDA = 3,        /* a CUDA runtime call failed; dp_last_error() names it */
+  DP_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait (device-side, in state.error) */
+} dp_status_t;
+
+/* Reduction arithmetic.  Both follow the same fixed order (see dp_step). */
+enum {
+  DP_SUM_COMPENSATED = 0, /* fp32 with Knuth's TwoSum error terms carried alongside */
+  DP_SUM_PLAIN = 1        /* plain fp32 additions */
+};
+
+/* ZeRO stages of the layout. */
+enum { DP_STAGE_DP = 0, DP_STAGE_ZERO1 = 1, DP_STAGE_ZERO2 = 2, DP_STAGE_ZERO3 = 3 };
+
+enum { DP_MAX_N = 16, DP_MAX_NA = 64, DP_MAX_SEG = 1024 };
+
+/* One contiguous piece of the flat parameter space [0, psi) and where its
+ * optimizer state lives: elements [global_off, global_off + len) are owned by
+ * rank `owner`, whose shard arrays hold them at [local_off, local_off + len). */
+typedef struct {
+  int64_t global_off;
+  int64_t len;       /* >= 0; empty pieces are allowed and ignored */
+  int32_t owner;     /* 0 <= owner < n */
+  int32_t reserved;  /* must be 0 */
+  int64_t local_off; /* >= 0 */
+} dp_segment_t;
+
+/* Shard layout (host memory).  Segments are sorted by global_off, contiguous,
+ * and cover [0, psi) exactly; one owner's local ranges must not overlap.
+ * stage 0 (plain data parallelism): every rank keeps full-length master/m/v
+ * arrays indexed by global position and the segments only fix each chunk's
+ * reduction order and where its averaged gradient is stored; stages 1-3:
+ * master/m/v of rank s are its shard arrays of dp_shard_len(layout, s)
+ * elements.  The stage does not change the arithmetic (ZeRO/FSDP paragraph:
+ * sharding changes layout and communication, not the update). */
+typedef struct {
+  int32_t stage;
+  int32_t n;        /* replicas, 1..DP_MAX_N */
+  int64_t psi;      /* parameters, >= 0 */
+  int32_t nseg;     /* 0..DP_MAX_SEG */
+  int32_t reserved; /* must be 0 */
+  const dp_segment_t* seg;
+} dp_layout_t;
+
+/* Adam hyper-parameters: lr >= 0, 0 <= beta < 1, eps > 0, all finite. */
+typedef struct {
+  float lr, beta1, beta2, eps;
+} dp_adam_t;
+
+/* Device-resident step state (64 bytes, 8-byte aligned, caller-allocated).
+ * Initialise with dp_state_init before the first step. */
+typedef struct {
+  int32_t t;          /* Adam steps applied so far */
+  int32_t found_inf;  /* 1 if the last reduction found a non-finite value: the step was skipped */
+  int32_t error;      /* sticky device-side error (DP_ERR_TIMEOUT) or 0; a set error skips every step */
+  int32_t reserved0;
+  uint64_t nonfinite; /* elements whose reduced gradient was not finite, last reduction */
+  double b1t, b2t;    /* beta1^t and beta2^t, running products */
+  uint64_t work_count;  /* kernel-internal, zero between calls */
+  uint32_t work_found;  /* kernel-internal, zero between calls */
+  uint32_t work_ticket; /* kernel-internal, zero between calls */
+  uint64_t reserved1;
+} dp_step_state_t;
+
+/* ---- host helpers (no GPU needed) --------------------------------------- */
+
+int32_t dp_abi_version(void);
+
+/* Name of a status code. */
+const char* dp_status_str(dp_status_t s);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* dp_last_error(void);
+
+/* Checks a layout against the rules of dp_layout_t.  DP_OK or DP_ERR_INVALID_ARG. */
+dp_status_t dp_layout_validate(const dp_layout_t* layout);
+
+/* Builds the standard layouts.  bucket <= 0: one bucket of psi elements.
+ * Each bucket is split n ways in rank order (the first (len mod n) pieces one
+ * element longer), every interior cut moved by +misalign elements (clamped),
+ * and each rank's pieces concatenated in its local space (FSDP units / DDP
+ * buckets, "FSDP wrapping granularity").  out may be NULL to query the count:
+ * *nseg is the capacity on entry and the number of segments on return. */
+dp_status_t dp_layout_even(int64_t psi, int32_t n, int64_t bucket, int32_t misalign, dp_segment_t* out,
+                           int32_t* nseg);
+
+/* Local length of rank's shard arrays (end of its furthest segment); -1 on error. */
+int64_t dp_shard_len(const dp_layout_t* layout, int32_t rank);
+
+/* Bytes of device workspace that dp_step needs when the caller passes ws
+ * instead of gbar_shard pointers: the n averaged-gradient shards, each
+ * 256-byte aligned.  0 on error. */
+size_t dp_workspace_size(const dp_layout_t* layout);
+
+/* Floats per rank in a dp_accumulate accumulator: psi (plain) or 2 psi
+ * (compensated, interleaved hi, lo). */
+size_t dp_acc_elems(int64_t psi, int32_t sum_mode);
+
+/* B_global = b x n x a: tensor and pipeline degrees are not multiplied in
+ * ("Distributed Training", data-parallel formula and 3D paragraph).  -1 on a
+ * negative input or overflow. */
+int64_t dp_global_batch(int64_t b, int32_t n, int32_t a);
+
+/* Model-state bytes per rank for mixed-precision Adam at 16 bytes per
+ * parameter (2 bf16 parameter, 2 bf16 gradient, 12 fp32 master + m + v;
+ * "Data vs Tensor vs Pipeline Parallelism", 16 bytes per parameter, ZeRO-3
+ * 16 Psi / N), stage 0-3 as in ZeRO: out[0] parameter bytes, out[1] gradient
+ * bytes, out[2] optimizer-state bytes, out[3] total.  Even split, fractional. */
+dp_status_t dp_memory_model(int32_t stage, int64_t psi, int32_t n, double out[4]);
+
+/* Ring traffic of one training step per rank with even shards: out[0] bytes
+ * sent (= received) per rank, out[1] ring steps, out[2] ratio to a plain-DP
+ * all-reduce of the gradient at the same wire size.  Stage 0: all-reduce of
+ * the gradient (2(N-1)/N x gradient bytes, 2(N-1) steps); stages 1-2:
+ * reduce-scatter of gradients + all-gather of parameters; stage 3: plus a
+ * second parameter all-gather for backward (1.5x when wire sizes match). */
+dp_status_t dp_traffic_model(int32_t stage, int64_t psi, int32_t n, int32_t wire_bytes_grad,
+                             int32_t wire_bytes_param, double out[3]);
+
+/* Upper bound, in nanoseconds, of every device-side wait of the kernels
+ * (default 2 s).  A wait that runs out records DP_ERR_TIMEOUT in
+ * state.error and the kernel returns; the step is skipped. */
+void dp_set_wait_timeout_ns(uint64_t ns);
+uint64_t dp_get_wait_timeout_ns(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t dp_kernel_launches(void);
+
+/* ---- device entry points -------------------------------------------------- */
+
+/* Sets *d_state to t = 0, beta powers 1, no skip, no error (one kernel). */
+dp_status_t dp_state_init(dp_step_state_t* d_state, dp_stream_t stream);
+
+/* Staged accumulation of one micro-step (data-parallel paragraphs: each rank
+ * sums its a micro-step gradients locally).  For every rank r < n:
+ *   first != 0:  acc[r] := g[r]          else  acc[r] += g[r]   (left to right)
+ * acc[r]: device, dp_acc_elems(psi, sum_mode) floats, element i at acc[r][i]
+ * (plain) or (hi, lo) at acc[r][2i], acc[r][2i+1] (compensated, TwoSum);
+ * g[r]: device, psi bf16. */
+dp_status_t dp_accumulate(float* const* acc, const uint16_t* const* g, int64_t psi, int32_t n, int32_t first,
+                          int32_t sum_mode, dp_stream_t stream);
+
+/* Staged reduce-scatter + average + unscale + non-finite check.  For each
+ * segment (owner s) and element i in it:
+ *   p = acc_{s+1} + acc_{s+2} + ... + acc_s   (ring order: the chunk starts at
+ *       rank s+1 and reaches its owner after n-1 hops; compensated mode adds
+ *       (hi, lo) pairs with TwoSum and ends with hi + lo)
+ *   gbar_shard[s][local_off + (i - global_off)] = fl32(p * fl32(1 / (n S)))
+ * then state.found_inf / state.nonfinite report whether any gbar is inf/NaN.
+ * gbar_shard[s]: device, dp_shard_len(layout, s) floats.  loss_scale S > 0. */
+dp_status_t dp_reduce_scatter_avg(float* const* gbar_shard, const float* const* acc, const dp_layout_t* layout,
+                                  float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream);
+
+/* Staged partitioned Adam.  Unless state.found_inf: t += 1, beta powers
+ * advance, then for every element of every shard (stage 0: of every rank's
+ * full arrays, with the owner's gbar):
+ *   m = b1 m + (1-b1) g ; v = b2 v + (1-b2) g^2 ;
+ *   theta -= (lr / (1 - b1^t)) m / (sqrt(v) / sqrt(1 - b2^t) + eps)
+ * master/m/v[s]: device fp32 shard arrays (stage 0: psi elements);
+ * gbar_shard[s]: as written by dp_reduce_scatter_avg. */
+dp_status_t dp_adam_shard(float* const* master, float* const* m, float* const* v, const float* const* gbar_shard,
+                          const dp_layout_t* layout, dp_adam_t adam, dp_step_state_t* d_state, dp_stream_t stream);
+
+/* Staged all-gather: unless state.found_inf, replicas[r][i] = bf16_rne(theta_i)
+ * for every rank r (stage 0: rank r's own master).  replicas[r]: device, psi bf16. */
+dp_status_t dp_allgather_params(uint16_t* const* replicas, const float* const* master, const dp_layout_t* layout,
+                                const dp_step_state_t* d_state, dp_stream_t stream);
+
+/* The fused step: dp_step_reduce then dp_step_update (two kernels).
+ * grads: host array of n*a device pointers, rank-major (grads[r*a + k] is
+ * micro-step k of rank r), each psi bf16.  Per element the gradient is summed
+ * in a fixed order -- micro-steps k = 0..a-1 within each rank, then ranks in
+ * ring order s+1, ..., s for the owner s -- so results are bit-identical run to
+ * run and identical to dp_accumulate + dp_reduce_scatter_avg + dp_adam_shard +
+ * dp_allgather_params.  gbar_shard: n device shards of dp_shard_len floats, or
+ * NULL to carve them from ws (dp_workspace_size bytes, 256-byte aligned).
+ * If any reduced value is not finite (or a wait timed out) master, m, v,
+ * replicas and t are left bit-for-bit unchanged. */
+dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                    const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                    float loss_scale, int32_t sum_mode, float* const* gbar_shard, void* ws,
+                    dp_step_state_t* d_state, dp_stream_t stream);
+
+/* First half of dp_step (one kernel): accumulate + ring reduce-scatter +
+ * average + unscale + non-finite check, gbar into the shards; the last CTA
+ * publishes found_inf / nonfinite and, unless found, advances t and the
+ * beta powers for the update that follows. */
+dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* const* grads, int32_t a,
+                           const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
+                           dp_step_state_t* d_state, dp_stream_t stream);
+
+/* Second half of dp_step (one kernel): unless found_inf, Adam on every shard
+ * and the bf16 all-gather into every replica, reading the gbar shards and the
+ * beta powers dp_step_reduce left. */
+dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                           const float* const* gbar_shard, void* ws, const dp_layout_t* layout, dp_adam_t adam,
+                           const dp_step_state_t* d_state, dp_stream_t stream);
+
+/* Reads found_inf and error of *d_state into host ints after synchronising
+ * the stream (the one blocking call).  skipped / err may be NULL. */
+dp_status_t dp_read_status(const dp_step_state_t* d_state, int32_t* skipped, int32_t* err, dp_stream_t stream);
+
+/* Self-test of the bounded wait: launches one block that waits on a barrier
+ * nothing will complete; after timeout_ns it records DP_ERR_TIMEOUT in
+ * d_state->error and returns, leaving the context usable. */
+dp_status_t dp_selftest_wait_timeout(dp_step_state_t* d_state, uint64_t timeout_ns, dp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPSTEP_H */

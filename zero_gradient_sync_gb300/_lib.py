@@ -1,0 +1,317 @@
+"""ctypes binding of libdpstep.so: the C entry points under the same names.
+
+Argument marshalling only -- tensors become device pointers, streams become
+cudaStream_t handles, layouts become dp_layout_t structs.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback: if the
+library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdpstep.so")
+
+DP_OK, DP_ERR_INVALID_ARG, DP_ERR_ALIGNMENT, DP_ERR_CUDA, DP_ERR_TIMEOUT = 0, 1, 2, 3, 4
+DP_SUM_COMPENSATED, DP_SUM_PLAIN = 0, 1
+DP_MAX_N, DP_MAX_NA, DP_MAX_SEG = 16, 64, 1024
+STATE_BYTES = 64
+
+c_i32, c_i64, c_u64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p
+
+
+class dp_segment_t(ctypes.Structure):
+    _fields_ = [("global_off", c_i64), ("len", c_i64), ("owner", c_i32), ("reserved", c_i32), ("local_off", c_i64)]
+
+
+class dp_layout_t(ctypes.Structure):
+    _fields_ = [("stage", c_i32), ("n", c_i32), ("psi", c_i64), ("nseg", c_i32), ("reserved", c_i32),
+                ("seg", ctypes.POINTER(dp_segment_t))]
+
+
+class dp_adam_t(ctypes.Structure):
+    _fields_ = [("lr", c_f32), ("beta1", c_f32), ("beta2", c_f32), ("eps", c_f32)]
+
+
+class dp_step_state_t(ctypes.Structure):
+    _fields_ = [("t", c_i32), ("found_inf", c_i32), ("error", c_i32), ("reserved0", c_i32), ("nonfinite", c_u64),
+                ("b1t", ctypes.c_double), ("b2t", ctypes.c_double), ("work_count", c_u64),
+                ("work_found", ctypes.c_uint32), ("work_ticket", ctypes.c_uint32), ("reserved1", c_u64)]
+
+
+assert ctypes.sizeof(dp_step_state_t) == STATE_BYTES
+assert ctypes.sizeof(dp_segment_t) == 32
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libdpstep.so is not built (run zero_gradient_sync_gb300.build.build()); "
+                          "there is no fallback path")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    sig = {
+        "dp_abi_version": (c_i32, []),
+        "dp_status_str": (ctypes.c_char_p, [c_i32]),
+        "dp_last_error": (ctypes.c_char_p, []),
+        "dp_layout_validate": (c_i32, [P(dp_layout_t)]),
+        "dp_layout_even": (c_i32, [c_i64, c_i32, c_i64, c_i32, P(dp_segment_t), P(c_i32)]),
+        "dp_shard_len": (c_i64, [P(dp_layout_t), c_i32]),
+        "dp_workspace_size": (ctypes.c_size_t, [P(dp_layout_t)]),
+        "dp_acc_elems": (ctypes.c_size_t, [c_i64, c_i32]),
+        "dp_global_batch": (c_i64, [c_i64, c_i32, c_i32]),
+        "dp_memory_model": (c_i32, [c_i32, c_i64, c_i32, P(ctypes.c_double)]),
+        "dp_traffic_model": (c_i32, [c_i32, c_i64, c_i32, c_i32, c_i32, P(ctypes.c_double)]),
+        "dp_set_wait_timeout_ns": (None, [c_u64]),
+        "dp_get_wait_timeout_ns": (c_u64, []),
+        "dp_kernel_launches": (c_u64, []),
+        "dp_state_init": (c_i32, [c_vp, c_vp]),
+        "dp_accumulate": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_vp]),
+        "dp_reduce_scatter_avg": (c_i32, [c_vp, c_vp, P(dp_layout_t), c_f32, c_i32, c_vp, c_vp]),
+        "dp_adam_shard": (c_i32, [c_vp, c_vp, c_vp, c_vp, P(dp_layout_t), dp_adam_t, c_vp, c_vp]),
+        "dp_allgather_params": (c_i32, [c_vp, c_vp, P(dp_layout_t), c_vp, c_vp]),
+        "dp_step": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32, c_vp,
+                            c_vp, c_vp, c_vp]),
+        "dp_step_reduce": (c_i32, [c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32, c_vp, c_vp]),
+        "dp_step_update": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, P(dp_layout_t), dp_adam_t, c_vp, c_vp]),
+        "dp_read_status": (c_i32, [c_vp, P(c_i32), P(c_i32), c_vp]),
+        "dp_selftest_wait_timeout": (c_i32, [c_vp, c_u64, c_vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+LIB = _load()
+
+
+class DPError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = LIB.dp_last_error().decode(errors="replace")
+        super().__init__("%s: %s (%s)" % (where, LIB.dp_status_str(code).decode(), msg))
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != DP_OK:
+        raise DPError(rc, where)
+
+
+# ------------------------------------------------------------------------------------------- marshalling
+
+def _ptr(t) -> int:
+    """Device address of a tensor (or an int address, or None -> NULL)."""
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _ptr_array(ts: Optional[Sequence]):
+    if ts is None:
+        return None
+    arr = (c_vp * max(1, len(ts)))(*[_ptr(t) for t in ts])
+    return arr
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_tensors(ts: Sequence, itemsize: int, min_numel: Sequence[int], name: str) -> None:
+    for i, t in enumerate(ts):
+        if isinstance(t, int):
+            continue
+        if not t.is_cuda:
+            raise ValueError("%s[%d] must be a CUDA tensor" % (name, i))
+        if not t.is_contiguous():
+            raise ValueError("%s[%d] must be contiguous" % (name, i))
+        if t.element_size() != itemsize:
+            raise ValueError("%s[%d]: element size %d, expected %d" % (name, i, t.element_size(), itemsize))
+        if t.numel() < min_numel[i]:
+            raise ValueError("%s[%d]: %d elements, need %d" % (name, i, t.numel(), min_numel[i]))
+
+
+class Layout:
+    """A dp_layout_t plus the segment array it points to (kept alive with it)."""
+
+    def __init__(self, stage: int, n: int, psi: int, segs: Sequence[Tuple[int, int, int, int]]):
+        self.stage, self.n, self.psi = int(stage), int(n), int(psi)
+        self.segs = [tuple(int(x) for x in s) for s in segs]
+        self._arr = (dp_segment_t * max(1, len(self.segs)))()
+        for k, (g, ln, o, lo) in enumerate(self.segs):
+            self._arr[k] = dp_segment_t(g, ln, o, 0, lo)
+        self.c = dp_layout_t(self.stage, self.n, self.psi, len(self.segs), 0,
+                             ctypes.cast(self._arr, ctypes.POINTER(dp_segment_t)))
+
+    @classmethod
+    def even(cls, psi: int, n: int, stage: int = 1, bucket: int = 0, misalign: int = 0) -> "Layout":
+        cnt = c_i32(0)
+        _check(LIB.dp_layout_even(psi, n, bucket, misalign, None, ctypes.byref(cnt)), "dp_layout_even")
+        arr = (dp_segment_t * max(1, cnt.value))()
+        _check(LIB.dp_layout_even(psi, n, bucket, misalign, arr, ctypes.byref(cnt)), "dp_layout_even")
+        return cls(stage, n, psi, [(arr[k].global_off, arr[k].len, arr[k].owner, arr[k].local_off)
+                                   for k in range(cnt.value)])
+
+    def validate(self) -> None:
+        _check(LIB.dp_layout_validate(ctypes.byref(self.c)), "dp_layout_validate")
+
+    def shard_len(self, rank: int) -> int:
+        v = LIB.dp_shard_len(ctypes.byref(self.c), rank)
+        if v < 0:
+            raise DPError(DP_ERR_INVALID_ARG, "dp_shard_len")
+        return int(v)
+
+    def shard_lens(self) -> List[int]:
+        return [self.shard_len(r) for r in range(self.n)]
+
+    def state_lens(self) -> List[int]:
+        """Length of each rank's master/m/v arrays: its shard, or psi for plain data parallelism."""
+        return [self.psi] * self.n if self.stage == 0 else self.shard_lens()
+
+    def workspace_size(self) -> int:
+        return int(LIB.dp_workspace_size(ctypes.byref(self.c)))
+
+
+def adam(lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8) -> dp_adam_t:
+    return dp_adam_t(lr, beta1, beta2, eps)
+
+
+# ------------------------------------------------------------------------------------------- entry points
+
+def dp_state_init(state, stream=None) -> None:
+    _check(LIB.dp_state_init(_ptr(state), _stream(stream)), "dp_state_init")
+
+
+def dp_accumulate(acc, g, psi: int, n: int, first: bool, sum_mode: int = DP_SUM_COMPENSATED, stream=None) -> None:
+    _check_tensors(acc, 4, [int(LIB.dp_acc_elems(psi, sum_mode))] * n, "acc")
+    _check_tensors(g, 2, [psi] * n, "g")
+    _check(LIB.dp_accumulate(_ptr_array(acc), _ptr_array(g), psi, n, 1 if first else 0, sum_mode, _stream(stream)),
+           "dp_accumulate")
+
+
+def dp_reduce_scatter_avg(gbar_shard, acc, layout: Layout, loss_scale: float, sum_mode: int, state,
+                          stream=None) -> None:
+    _check_tensors(gbar_shard, 4, layout.shard_lens(), "gbar_shard")
+    _check_tensors(acc, 4, [int(LIB.dp_acc_elems(layout.psi, sum_mode))] * layout.n, "acc")
+    _check(LIB.dp_reduce_scatter_avg(_ptr_array(gbar_shard), _ptr_array(acc), ctypes.byref(layout.c), loss_scale,
+                                     sum_mode, _ptr(state), _stream(stream)), "dp_reduce_scatter_avg")
+
+
+def dp_adam_shard(master, m, v, gbar_shard, layout: Layout, adam_: dp_adam_t, state, stream=None) -> None:
+    lens = layout.state_lens()
+    for name, ts in (("master", master), ("m", m), ("v", v)):
+        _check_tensors(ts, 4, lens, name)
+    _check_tensors(gbar_shard, 4, layout.shard_lens(), "gbar_shard")
+    _check(LIB.dp_adam_shard(_ptr_array(master), _ptr_array(m), _ptr_array(v), _ptr_array(gbar_shard),
+                             ctypes.byref(layout.c), adam_, _ptr(state), _stream(stream)), "dp_adam_shard")
+
+
+def dp_allgather_params(replicas, master, layout: Layout, state, stream=None) -> None:
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    _check_tensors(master, 4, layout.state_lens(), "master")
+    _check(LIB.dp_allgather_params(_ptr_array(replicas), _ptr_array(master), ctypes.byref(layout.c), _ptr(state),
+                                   _stream(stream)), "dp_allgather_params")
+
+
+def _gbar_args(layout: Layout, gbar_shard, ws):
+    if gbar_shard is not None:
+        _check_tensors(gbar_shard, 4, layout.shard_lens(), "gbar_shard")
+    if ws is not None and not isinstance(ws, int) and ws.numel() * ws.element_size() < layout.workspace_size():
+        raise ValueError("workspace smaller than dp_workspace_size")
+    return _ptr_array(gbar_shard), _ptr(ws)
+
+
+def dp_step(replicas, master, m, v, grads, a: int, layout: Layout, adam_: dp_adam_t, loss_scale: float,
+            sum_mode: int = DP_SUM_COMPENSATED, gbar_shard=None, ws=None, state=None, stream=None) -> None:
+    lens = layout.state_lens()
+    for name, ts in (("master", master), ("m", m), ("v", v)):
+        _check_tensors(ts, 4, lens, name)
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    _check_tensors(grads, 2, [layout.psi] * len(grads), "grads")
+    gb, w = _gbar_args(layout, gbar_shard, ws)
+    _check(LIB.dp_step(_ptr_array(replicas), _ptr_array(master), _ptr_array(m), _ptr_array(v), _ptr_array(grads), a,
+                       ctypes.byref(layout.c), adam_, loss_scale, sum_mode, gb, w, _ptr(state), _stream(stream)),
+           "dp_step")
+
+
+def dp_step_reduce(gbar_shard, ws, grads, a: int, layout: Layout, adam_: dp_adam_t, loss_scale: float,
+                   sum_mode: int, state, stream=None) -> None:
+    _check_tensors(grads, 2, [layout.psi] * len(grads), "grads")
+    gb, w = _gbar_args(layout, gbar_shard, ws)
+    _check(LIB.dp_step_reduce(gb, w, _ptr_array(grads), a, ctypes.byref(layout.c), adam_, loss_scale, sum_mode,
+                              _ptr(state), _stream(stream)), "dp_step_reduce")
+
+
+def dp_step_update(replicas, master, m, v, gbar_shard, ws, layout: Layout, adam_: dp_adam_t, state,
+                   stream=None) -> None:
+    lens = layout.state_lens()
+    for name, ts in (("master", master), ("m", m), ("v", v)):
+        _check_tensors(ts, 4, lens, name)
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    gb, w = _gbar_args(layout, gbar_shard, ws)
+    _check(LIB.dp_step_update(_ptr_array(replicas), _ptr_array(master), _ptr_array(m), _ptr_array(v), gb, w,
+                              ctypes.byref(layout.c), adam_, _ptr(state), _stream(stream)), "dp_step_update")
+
+
+def dp_read_status(state, stream=None) -> Tuple[int, int]:
+    sk, er = c_i32(0), c_i32(0)
+    _check(LIB.dp_read_status(_ptr(state), ctypes.byref(sk), ctypes.byref(er), _stream(stream)), "dp_read_status")
+    return int(sk.value), int(er.value)
+
+
+def dp_selftest_wait_timeout(state, timeout_ns: int, stream=None) -> None:
+    _check(LIB.dp_selftest_wait_timeout(_ptr(state), timeout_ns, _stream(stream)), "dp_selftest_wait_timeout")
+
+
+def dp_global_batch(b: int, n: int, a: int) -> int:
+    return int(LIB.dp_global_batch(b, n, a))
+
+
+def dp_memory_model(stage: int, psi: int, n: int) -> List[float]:
+    out = (ctypes.c_double * 4)()
+    _check(LIB.dp_memory_model(stage, psi, n, out), "dp_memory_model")
+    return list(out)
+
+
+def dp_traffic_model(stage: int, psi: int, n: int, wire_bytes_grad: int, wire_bytes_param: int) -> List[float]:
+    out = (ctypes.c_double * 3)()
+    _check(LIB.dp_traffic_model(stage, psi, n, wire_bytes_grad, wire_bytes_param, out), "dp_traffic_model")
+    return list(out)
+
+
+def dp_kernel_launches() -> int:
+    return int(LIB.dp_kernel_launches())
+
+
+def dp_set_wait_timeout_ns(ns: int) -> None:
+    LIB.dp_set_wait_timeout_ns(ns)
+
+
+def dp_get_wait_timeout_ns() -> int:
+    return int(LIB.dp_get_wait_timeout_ns())
+
+
+def new_state(device=None):
+    """A 64-byte device state buffer, initialised (t = 0)."""
+    import torch
+    st = torch.zeros(STATE_BYTES, dtype=torch.uint8, device=device or "cuda")
+    dp_state_init(st)
+    return st
+
+
+def read_state(state) -> dict:
+    """Decodes a device state buffer (copies it to the host)."""
+    raw = bytes(state.detach().cpu().numpy().tobytes())
+    s = dp_step_state_t.from_buffer_copy(raw)
+    return {"t": s.t, "found_inf": s.found_inf, "error": s.error, "nonfinite": s.nonfinite, "b1t": s.b1t,
+            "b2t": s.b2t, "work_count": s.work_count, "work_found": s.work_found, "work_ticket": s.work_ticket}

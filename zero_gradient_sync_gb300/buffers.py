@@ -1,0 +1,58 @@
+"""Device buffers of one data-parallel step, allocated with PyTorch (memory and streams only).
+
+StepBuffers holds, for a layout of n replicas and a micro-steps: the n*a bf16 gradient buffers (rank-major),
+the n bf16 parameter replicas, each rank's fp32 master/m/v arrays (its shard, or full length for plain data
+parallelism), the n fp32 averaged-gradient shards and the 64-byte device step state.  Every tensor is a
+separate allocation, so every base pointer is 256-byte aligned.
+"""
+from __future__ import annotations
+
+from typing import List, Optional
+
+import torch
+
+from . import _lib
+from ._lib import DP_SUM_COMPENSATED, Layout
+
+
+class StepBuffers:
+    def __init__(self, layout: Layout, a: int, device=None, with_grads: bool = True):
+        self.layout = layout
+        self.n, self.a, self.psi = layout.n, int(a), layout.psi
+        self.device = torch.device(device or "cuda")
+        dev = self.device
+        lens = layout.state_lens()
+        shard = layout.shard_lens()
+        self.grads: List[torch.Tensor] = (
+            [torch.empty(self.psi, dtype=torch.bfloat16, device=dev) for _ in range(self.n * self.a)]
+            if with_grads else [])
+        self.replicas = [torch.empty(self.psi, dtype=torch.bfloat16, device=dev) for _ in range(self.n)]
+        self.master = [torch.empty(L, dtype=torch.float32, device=dev) for L in lens]
+        self.m = [torch.zeros(L, dtype=torch.float32, device=dev) for L in lens]
+        self.v = [torch.zeros(L, dtype=torch.float32, device=dev) for L in lens]
+        self.gbar = [torch.empty(L, dtype=torch.float32, device=dev) for L in shard]
+        self.state = _lib.new_state(dev)
+
+    def grad(self, r: int, k: int) -> torch.Tensor:
+        return self.grads[r * self.a + k]
+
+    def step(self, adam_: _lib.dp_adam_t, loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED,
+             stream=None) -> None:
+        _lib.dp_step(self.replicas, self.master, self.m, self.v, self.grads, self.a, self.layout, adam_,
+                     loss_scale, sum_mode, gbar_shard=self.gbar, state=self.state, stream=stream)
+
+    def reduce(self, adam_: _lib.dp_adam_t, loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED,
+               stream=None) -> None:
+        _lib.dp_step_reduce(self.gbar, None, self.grads, self.a, self.layout, adam_, loss_scale, sum_mode,
+                            self.state, stream=stream)
+
+    def update(self, adam_: _lib.dp_adam_t, stream=None) -> None:
+        _lib.dp_step_update(self.replicas, self.master, self.m, self.v, self.gbar, None, self.layout, adam_,
+                            self.state, stream=stream)
+
+    def status(self, stream=None):
+        return _lib.dp_read_status(self.state, stream=stream)
+
+    def nbytes(self) -> int:
+        ts = self.grads + self.replicas + self.master + self.m + self.v + self.gbar
+        return sum(t.numel() * t.element_size() for t in ts) + _lib.STATE_BYTES

@@ -1,0 +1,466 @@
+// C ABI of the fused data-parallel step: argument checks, layout plans and
+// the launch sequences.  Every check runs before the first launch, so a call
+// that returns an argument error has launched nothing.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "dp_device.cuh"
+#include "dp_internal.h"
+#include "dpstep.h"
+
+using dp::Plan;
+using dp::StepScalars;
+
+namespace {
+
+thread_local char g_err[512] = "";
+std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+dp_status_t fail(dp_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+dp_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(DP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct LaunchCount {
+  uint64_t n = 0;
+  ~LaunchCount() { g_launches.fetch_add(n); }
+};
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+dp_status_t check_ptr_array(const void* const* arr, int count, const char* name) {
+  if (!arr) return fail(DP_ERR_INVALID_ARG, "%s: pointer array is NULL", name);
+  for (int i = 0; i < count; ++i) {
+    if (!arr[i]) return fail(DP_ERR_INVALID_ARG, "%s[%d] is NULL", name, i);
+    if (!aligned16(arr[i])) return fail(DP_ERR_ALIGNMENT, "%s[%d] is not 16-byte aligned", name, i);
+  }
+  return DP_OK;
+}
+
+dp_status_t check_state(const void* st) {
+  if (!st) return fail(DP_ERR_INVALID_ARG, "state is NULL");
+  if (((uintptr_t)st & 7u) != 0) return fail(DP_ERR_ALIGNMENT, "state is not 8-byte aligned");
+  return DP_OK;
+}
+
+dp_status_t build_plan(const dp_layout_t* L, Plan& P) {
+  if (!L) return fail(DP_ERR_INVALID_ARG, "layout is NULL");
+  if (L->stage < 0 || L->stage > 3) return fail(DP_ERR_INVALID_ARG, "stage %d not in 0..3", L->stage);
+  if (L->n < 1 || L->n > DP_MAX_N) return fail(DP_ERR_INVALID_ARG, "n = %d not in 1..%d", L->n, DP_MAX_N);
+  if (L->psi < 0) return fail(DP_ERR_INVALID_ARG, "psi < 0");
+  if (L->nseg < 0 || L->nseg > DP_MAX_SEG)
+    return fail(DP_ERR_INVALID_ARG, "nseg = %d not in 0..%d", L->nseg, DP_MAX_SEG);
+  if (L->reserved != 0) return fail(DP_ERR_INVALID_ARG, "layout.reserved must be 0");
+  if (L->nseg > 0 && !L->seg) return fail(DP_ERR_INVALID_ARG, "layout.seg is NULL");
+  P.n = L->n;
+  P.stage = L->stage;
+  P.psi = L->psi;
+  for (int r = 0; r < DP_MAX_N; ++r) P.shard_len[r] = 0;
+  struct LR {
+    int32_t owner;
+    int64_t lo, len;
+  };
+  std::vector<LR> locals;
+  locals.reserve(L->nseg);
+  int64_t g = 0;
+  int k = 0;
+  int64_t tiles = 0;
+  for (int i = 0; i < L->nseg; ++i) {
+    const dp_segment_t& s = L->seg[i];
+    if (s.reserved != 0) return fail(DP_ERR_INVALID_ARG, "seg[%d].reserved must be 0", i);
+    if (s.global_off != g)
+      return fail(DP_ERR_INVALID_ARG, "seg[%d].global_off = %lld, expected %lld (segments must be contiguous)", i,
+                  (long long)s.global_off, (long long)g);
+    if (s.len < 0 || s.len > L->psi - g) return fail(DP_ERR_INVALID_ARG, "seg[%d].len out of range", i);
+    if (s.owner < 0 || s.owner >= L->n) return fail(DP_ERR_INVALID_ARG, "seg[%d].owner = %d not in 0..n-1", i, s.owner);
+    if (s.local_off < 0 || s.local_off > INT64_MAX / 2 - s.len)
+      return fail(DP_ERR_INVALID_ARG, "seg[%d].local_off out of range", i);
+    g += s.len;
+    if (s.len == 0) continue;
+    locals.push_back({s.owner, s.local_off, s.len});
+    P.shard_len[s.owner] = std::max(P.shard_len[s.owner], s.local_off + s.len);
+    const int64_t gend = s.global_off + s.len;
+    const int64_t nt = (gend + dp::TILE - 1) / dp::TILE - s.global_off / dp::TILE;
+    P.e[k].goff = s.global_off;
+    P.e[k].loff = s.local_off;
+    P.e[k].owner = s.owner;
+    P.e[k].tile0 = (int32_t)tiles;
+    tiles += nt;
+    if (tiles > INT32_MAX) return fail(DP_ERR_INVALID_ARG, "too many tiles");
+    ++k;
+  }
+  if (g != L->psi) return fail(DP_ERR_INVALID_ARG, "segments cover %lld of psi = %lld elements", (long long)g,
+                               (long long)L->psi);
+  std::sort(locals.begin(), locals.end(), [](const LR& x, const LR& y) {
+    return x.owner != y.owner ? x.owner < y.owner : x.lo < y.lo;
+  });
+  for (size_t i = 1; i < locals.size(); ++i)
+    if (locals[i].owner == locals[i - 1].owner && locals[i].lo < locals[i - 1].lo + locals[i - 1].len)
+      return fail(DP_ERR_INVALID_ARG, "rank %d: local ranges overlap", locals[i].owner);
+  P.nseg = k;
+  P.ntiles = (int32_t)tiles;
+  P.e[k].goff = L->psi;
+  P.e[k].loff = 0;
+  P.e[k].owner = 0;
+  P.e[k].tile0 = (int32_t)tiles;
+  return DP_OK;
+}
+
+dp_status_t check_adam(const dp_adam_t& A) {
+  if (!std::isfinite(A.lr) || A.lr < 0.0f) return fail(DP_ERR_INVALID_ARG, "lr must be finite and >= 0");
+  if (!(A.beta1 >= 0.0f && A.beta1 < 1.0f)) return fail(DP_ERR_INVALID_ARG, "beta1 must be in [0, 1)");
+  if (!(A.beta2 >= 0.0f && A.beta2 < 1.0f)) return fail(DP_ERR_INVALID_ARG, "beta2 must be in [0, 1)");
+  if (!std::isfinite(A.eps) || !(A.eps > 0.0f)) return fail(DP_ERR_INVALID_ARG, "eps must be finite and > 0");
+  return DP_OK;
+}
+
+dp_status_t scalars(const Plan& P, const dp_adam_t* A, float loss_scale, int sum_mode, StepScalars& s) {
+  if (sum_mode != DP_SUM_COMPENSATED && sum_mode != DP_SUM_PLAIN)
+    return fail(DP_ERR_INVALID_ARG, "sum_mode %d unknown", sum_mode);
+  if (!std::isfinite(loss_scale) || !(loss_scale > 0.0f))
+    return fail(DP_ERR_INVALID_ARG, "loss scale must be finite and > 0");
+  const double inv = 1.0 / ((double)P.n * (double)loss_scale);
+  const float inv32 = (float)inv;
+  if (!std::isfinite(inv32) || !(inv32 >= 1.17549435e-38f))
+    return fail(DP_ERR_INVALID_ARG, "1 / (n * loss_scale) is not a normal fp32 number");
+  s.inv = inv32;
+  s.mode = sum_mode;
+  s.timeout_ns = g_timeout_ns.load();
+  if (A) {
+    dp_status_t st = check_adam(*A);
+    if (st != DP_OK) return st;
+    s.lr = A->lr;
+    s.beta1 = A->beta1;
+    s.beta2 = A->beta2;
+    s.eps = A->eps;
+    s.omb1 = (float)(1.0 - (double)A->beta1);
+    s.omb2 = (float)(1.0 - (double)A->beta2);
+  } else {
+    s.lr = s.beta1 = s.beta2 = s.eps = s.omb1 = s.omb2 = 0.0f;
+  }
+  return DP_OK;
+}
+
+size_t align256(size_t x) { return (x + 255u) & ~size_t(255u); }
+
+// gbar shard pointers: the caller's, or carved from ws.
+dp_status_t gbar_ptrs(const Plan& P, float* const* gbar_shard, void* ws, float** out) {
+  if (gbar_shard) {
+    for (int r = 0; r < P.n; ++r) out[r] = gbar_shard[r];
+    return check_ptr_array((const void* const*)out, P.n, "gbar_shard");
+  }
+  if (!ws) return fail(DP_ERR_INVALID_ARG, "both gbar_shard and ws are NULL");
+  if (((uintptr_t)ws & 255u) != 0) return fail(DP_ERR_ALIGNMENT, "ws is not 256-byte aligned");
+  size_t off = 0;
+  for (int r = 0; r < P.n; ++r) {
+    out[r] = reinterpret_cast<float*>(static_cast<char*>(ws) + off);
+    off += align256((size_t)P.shard_len[r] * sizeof(float));
+  }
+  return DP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dp_abi_version(void) { return 1; }
+
+const char* dp_status_str(dp_status_t s) {
+  switch (s) {
+    case DP_OK: return "DP_OK";
+    case DP_ERR_INVALID_ARG: return "DP_ERR_INVALID_ARG";
+    case DP_ERR_ALIGNMENT: return "DP_ERR_ALIGNMENT";
+    case DP_ERR_CUDA: return "DP_ERR_CUDA";
+    case DP_ERR_TIMEOUT: return "DP_ERR_TIMEOUT";
+  }
+  return "DP_ERR_UNKNOWN";
+}
+
+const char* dp_last_error(void) { return g_err; }
+
+dp_status_t dp_layout_validate(const dp_layout_t* layout) {
+  static thread_local Plan P;
+  return build_plan(layout, P);
+}
+
+dp_status_t dp_layout_even(int64_t psi, int32_t n, int64_t bucket, int32_t misalign, dp_segment_t* out,
+                           int32_t* nseg) {
+  if (!nseg) return fail(DP_ERR_INVALID_ARG, "nseg is NULL");
+  if (psi < 0 || n < 1 || n > DP_MAX_N || misalign < 0) return fail(DP_ERR_INVALID_ARG, "bad psi, n or misalign");
+  if (bucket <= 0 || bucket > psi) bucket = psi > 0 ? psi : 1;
+  const int64_t nb = psi == 0 ? 0 : (psi + bucket - 1) / bucket;
+  if (nb * n > DP_MAX_SEG) return fail(DP_ERR_INVALID_ARG, "%lld segments exceed %d", (long long)(nb * n), DP_MAX_SEG);
+  const int32_t count = (int32_t)(nb * n);
+  if (out) {
+    if (*nseg < count) return fail(DP_ERR_INVALID_ARG, "capacity %d < %d segments", *nseg, count);
+    std::vector<int64_t> local(n, 0), cuts(n + 1);
+    int idx = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+      const int64_t b0 = b * bucket;
+      const int64_t len = std::min(bucket, psi - b0);
+      const int64_t base = len / n, extra = len % n;
+      for (int k = 0; k <= n; ++k) cuts[k] = k * base + std::min<int64_t>(k, extra);
+      for (int k = 1; k < n; ++k) cuts[k] = std::min(len, cuts[k] + misalign);
+      for (int k = 1; k <= n; ++k) cuts[k] = std::max(cuts[k], cuts[k - 1]);
+      for (int s = 0; s < n; ++s) {
+        dp_segment_t& e = out[idx++];
+        e.global_off = b0 + cuts[s];
+        e.len = cuts[s + 1] - cuts[s];
+        e.owner = s;
+        e.reserved = 0;
+        e.local_off = local[s];
+        local[s] += e.len;
+      }
+    }
+  }
+  *nseg = count;
+  return DP_OK;
+}
+
+int64_t dp_shard_len(const dp_layout_t* layout, int32_t rank) {
+  static thread_local Plan P;
+  if (build_plan(layout, P) != DP_OK || rank < 0 || rank >= P.n) return -1;
+  return P.shard_len[rank];
+}
+
+size_t dp_workspace_size(const dp_layout_t* layout) {
+  static thread_local Plan P;
+  if (build_plan(layout, P) != DP_OK) return 0;
+  size_t off = 0;
+  for (int r = 0; r < P.n; ++r) off += align256((size_t)P.shard_len[r] * sizeof(float));
+  return off > 0 ? off : 256;
+}
+
+size_t dp_acc_elems(int64_t psi, int32_t sum_mode) {
+  if (psi < 0) return 0;
+  return (size_t)psi * (sum_mode == DP_SUM_COMPENSATED ? 2u : 1u);
+}
+
+int64_t dp_global_batch(int64_t b, int32_t n, int32_t a) {
+  if (b < 0 || n < 0 || a < 0) return -1;
+  const long double x = (long double)b * n * a;
+  if (x > (long double)INT64_MAX) return -1;
+  return b * (int64_t)n * (int64_t)a;
+}
+
+dp_status_t dp_memory_model(int32_t stage, int64_t psi, int32_t n, double out[4]) {
+  if (!out || stage < 0 || stage > 3 || psi < 0 || n < 1) return fail(DP_ERR_INVALID_ARG, "bad memory-model args");
+  const double P = (double)psi, N = (double)n;
+  double params = 2.0 * P, grads = 2.0 * P, opt = 12.0 * P;
+  if (stage >= 1) opt /= N;
+  if (stage >= 2) grads /= N;
+  if (stage >= 3) params /= N;
+  out[0] = params;
+  out[1] = grads;
+  out[2] = opt;
+  out[3] = params + grads + opt;
+  return DP_OK;
+}
+
+dp_status_t dp_traffic_model(int32_t stage, int64_t psi, int32_t n, int32_t wire_bytes_grad,
+                             int32_t wire_bytes_param, double out[3]) {
+  if (!out || stage < 0 || stage > 3 || psi < 0 || n < 1 || wire_bytes_grad < 1 || wire_bytes_param < 1)
+    return fail(DP_ERR_INVALID_ARG, "bad traffic-model args");
+  const double f = (double)(n - 1) / (double)n * (double)psi;
+  const double wg = wire_bytes_grad, wp = wire_bytes_param;
+  double per = 0.0, units = 0.0;  // bytes per rank, and the same in units of f * wg
+  int phases = 0;
+  if (stage == 0) {
+    per = 2.0 * f * wg;
+    units = 2.0;
+    phases = 2;
+  } else if (stage <= 2) {
+    per = f * (wg + wp);
+    units = (wg + wp) / wg;
+    phases = 2;
+  } else {
+    per = f * (wg + 2.0 * wp);
+    units = (wg + 2.0 * wp) / wg;
+    phases = 3;
+  }
+  out[0] = per;
+  out[1] = (double)phases * (double)(n - 1);
+  out[2] = units / 2.0;
+  return DP_OK;
+}
+
+void dp_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 1); }
+uint64_t dp_get_wait_timeout_ns(void) { return g_timeout_ns.load(); }
+uint64_t dp_kernel_launches(void) { return g_launches.load(); }
+
+dp_status_t dp_state_init(dp_step_state_t* d_state, dp_stream_t stream) {
+  dp_status_t st = check_state(d_state);
+  if (st != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_state_init(d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "state_init launch");
+}
+
+dp_status_t dp_accumulate(float* const* acc, const uint16_t* const* g, int64_t psi, int32_t n, int32_t first,
+                          int32_t sum_mode, dp_stream_t stream) {
+  if (psi < 0 || n < 1 || n > DP_MAX_N) return fail(DP_ERR_INVALID_ARG, "bad psi or n");
+  if (sum_mode != DP_SUM_COMPENSATED && sum_mode != DP_SUM_PLAIN)
+    return fail(DP_ERR_INVALID_ARG, "sum_mode %d unknown", sum_mode);
+  dp_status_t st = check_ptr_array((const void* const*)acc, n, "acc");
+  if (st == DP_OK) st = check_ptr_array((const void* const*)g, n, "g");
+  if (st != DP_OK) return st;
+  if (psi == 0) return DP_OK;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_accumulate(acc, g, psi, n, first, sum_mode, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "accumulate launch");
+}
+
+dp_status_t dp_reduce_scatter_avg(float* const* gbar_shard, const float* const* acc, const dp_layout_t* layout,
+                                  float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  StepScalars s;
+  if ((st = scalars(P, nullptr, loss_scale, sum_mode, s)) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)gbar_shard, P.n, "gbar_shard")) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)acc, P.n, "acc")) != DP_OK) return st;
+  if ((st = check_state(d_state)) != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_rs_avg(P, acc, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "reduce_scatter_avg launch");
+}
+
+static dp_status_t check_state_arrays(const Plan& P, float* const* master, float* const* m, float* const* v) {
+  dp_status_t st = check_ptr_array((const void* const*)master, P.n, "master");
+  if (st == DP_OK) st = check_ptr_array((const void* const*)m, P.n, "m");
+  if (st == DP_OK) st = check_ptr_array((const void* const*)v, P.n, "v");
+  return st;
+}
+
+dp_status_t dp_adam_shard(float* const* master, float* const* m, float* const* v, const float* const* gbar_shard,
+                          const dp_layout_t* layout, dp_adam_t adam, dp_step_state_t* d_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  StepScalars s;
+  if ((st = scalars(P, &adam, 1.0f, DP_SUM_COMPENSATED, s)) != DP_OK) return st;
+  if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)gbar_shard, P.n, "gbar_shard")) != DP_OK) return st;
+  if ((st = check_state(d_state)) != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_advance(d_state, (double)adam.beta1, (double)adam.beta2, (cudaStream_t)stream, &lc.n);
+  if (e != cudaSuccess) return cuda_fail(e, "advance launch");
+  e = dp::launch_update(P, nullptr, master, m, v, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "adam launch");
+}
+
+dp_status_t dp_allgather_params(uint16_t* const* replicas, const float* const* master, const dp_layout_t* layout,
+                                const dp_step_state_t* d_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)master, P.n, "master")) != DP_OK) return st;
+  if ((st = check_state(d_state)) != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_allgather(P, replicas, master, d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "allgather launch");
+}
+
+static dp_status_t prepare_reduce(const Plan& P, const uint16_t* const* grads, int32_t a, const dp_adam_t& adam,
+                                  float loss_scale, int32_t sum_mode, float* const* gbar_shard, void* ws,
+                                  dp_step_state_t* d_state, StepScalars& s, float** gb) {
+  if (a < 1 || (int64_t)a * P.n > DP_MAX_NA)
+    return fail(DP_ERR_INVALID_ARG, "a = %d: need 1 <= a and n * a <= %d", a, DP_MAX_NA);
+  dp_status_t st = scalars(P, &adam, loss_scale, sum_mode, s);
+  if (st == DP_OK) st = check_ptr_array((const void* const*)grads, P.n * a, "grads");
+  if (st == DP_OK) st = gbar_ptrs(P, gbar_shard, ws, gb);
+  if (st == DP_OK) st = check_state(d_state);
+  return st;
+}
+
+dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* const* grads, int32_t a,
+                           const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
+                           dp_step_state_t* d_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  StepScalars s;
+  float* gb[DP_MAX_N];
+  if ((st = prepare_reduce(P, grads, a, adam, loss_scale, sum_mode, gbar_shard, ws, d_state, s, gb)) != DP_OK)
+    return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_reduce(P, grads, a, gb, s, 1, d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "reduce launch");
+}
+
+dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                           const float* const* gbar_shard, void* ws, const dp_layout_t* layout, dp_adam_t adam,
+                           const dp_step_state_t* d_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  StepScalars s;
+  if ((st = scalars(P, &adam, 1.0f, DP_SUM_COMPENSATED, s)) != DP_OK) return st;
+  if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  float* gb[DP_MAX_N];
+  if ((st = gbar_ptrs(P, (float* const*)gbar_shard, ws, gb)) != DP_OK) return st;
+  if ((st = check_state(d_state)) != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
+}
+
+dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                    const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                    float loss_scale, int32_t sum_mode, float* const* gbar_shard, void* ws,
+                    dp_step_state_t* d_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  StepScalars s;
+  float* gb[DP_MAX_N];
+  if ((st = prepare_reduce(P, grads, a, adam, loss_scale, sum_mode, gbar_shard, ws, d_state, s, gb)) != DP_OK)
+    return st;
+  if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_reduce(P, grads, a, gb, s, 1, d_state, (cudaStream_t)stream, &lc.n);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
+  e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
+}
+
+dp_status_t dp_read_status(const dp_step_state_t* d_state, int32_t* skipped, int32_t* err, dp_stream_t stream) {
+  dp_status_t st = check_state(d_state);
+  if (st != DP_OK) return st;
+  dp_step_state_t h;
+  cudaError_t e = cudaMemcpyAsync(&h, d_state, sizeof(h), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "read_status copy");
+  e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "read_status sync");
+  if (skipped) *skipped = h.found_inf;
+  if (err) *err = h.error;
+  return DP_OK;
+}
+
+dp_status_t dp_selftest_wait_timeout(dp_step_state_t* d_state, uint64_t timeout_ns, dp_stream_t stream) {
+  dp_status_t st = check_state(d_state);
+  if (st != DP_OK) return st;
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull)
+    return fail(DP_ERR_INVALID_ARG, "timeout_ns must be in (0, 10 s]");
+  LaunchCount lc;
+  cudaError_t e = dp::launch_selftest_wait(d_state, timeout_ns, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "selftest launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,245 @@
+// Device-side building blocks of the fused data-parallel step (sm_103a).
+//
+// Work decomposition shared by every kernel: the non-empty segments of a
+// layout are cut on the global grid of TILE elements, so a tile never
+// crosses a segment (owner) boundary and never crosses a TILE cell.  A
+// tile's aligned hull [floor8(start), ceil8(end)) therefore stays inside
+// its cell, which keeps every bulk copy 16-byte aligned.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dpstep.h"
+
+namespace dp {
+
+constexpr int TILE = 4096;          // elements per tile, multiple of 8
+constexpr int SMALL_SEG = 32;       // segment-table capacity of the small kernel variants
+constexpr int BIG_SEG = DP_MAX_SEG; // ... and of the large ones
+
+struct SegEntry {
+  int64_t goff;   // first global element of the segment
+  int64_t loff;   // first local element in the owner's shard arrays
+  int32_t tile0;  // index of the segment's first tile
+  int32_t owner;
+};
+
+// Passed by value inside kernel parameters (__grid_constant__): e[nseg] is a
+// sentinel with goff = psi and tile0 = ntiles.
+template <int MAXSEG>
+struct SegTable {
+  int64_t psi;
+  int32_t nseg;
+  int32_t ntiles;
+  SegEntry e[MAXSEG + 1];
+};
+
+struct Tile {
+  int64_t goff, loff, start, end;  // segment origin (global, local) and the tile's global range
+  int32_t owner;
+};
+
+template <int MAXSEG>
+__device__ __forceinline__ Tile tile_at(const SegTable<MAXSEG>& T, int tile) {
+  int lo = 0, hi = T.nseg - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (T.e[mid].tile0 <= tile) lo = mid; else hi = mid - 1;
+  }
+  const int64_t goff = T.e[lo].goff;
+  const int64_t gend = T.e[lo + 1].goff;
+  const int64_t cell = goff / TILE + (tile - T.e[lo].tile0);
+  Tile t;
+  t.goff = goff;
+  t.loff = T.e[lo].loff;
+  t.owner = T.e[lo].owner;
+  t.start = goff > cell * TILE ? goff : cell * TILE;
+  t.end = gend < (cell + 1) * TILE ? gend : (cell + 1) * TILE;
+  return t;
+}
+
+// ---------------------------------------------------------------- fp32 arithmetic
+
+__device__ __forceinline__ bool nonfinite(float x) {
+  return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// Knuth's TwoSum (TAOCP vol. 2, 4.2.2): s = fl(a + b) and e with s + e = a + b exactly.
+__device__ __forceinline__ float two_sum(float a, float b, float& e) {
+  const float s = __fadd_rn(a, b);
+  const float z = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+  return s;
+}
+
+// Packed pairs of fp32 for the sm_100+ f32x2 instructions: two independent
+// round-to-nearest operations per instruction, bit-identical to the scalar ones.
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+  f2_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
+  f2_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+  f2_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t f2_two_sum(f2_t a, f2_t b, f2_t& e) {
+  const f2_t s = f2_add(a, b);
+  const f2_t z = f2_sub(s, a);
+  e = f2_add(f2_sub(a, f2_sub(s, z)), f2_sub(b, z));
+  return s;
+}
+__device__ __forceinline__ f2_t bf16x2_to_f2(uint32_t w) { return f2_pack(bf16_lo(w), bf16_hi(w)); }
+
+// ---------------------------------------------------------------- Adam
+
+struct AdamK {
+  float b1, b2, omb1, omb2, eps;
+  float step;   // fl32(lr / (1 - beta1^t))
+  float rsbc2;  // fl32(1 / sqrt(1 - beta2^t))
+};
+
+// One Adam update in fp32, every operation rounded once (no contraction):
+//   m' = b1 m + (1-b1) g ; v' = b2 v + ((1-b2) g) g
+//   th' = th - (step m') / (sqrt(v') rsbc2 + eps)
+__device__ __forceinline__ void adam1(float g, float& th, float& m, float& v, const AdamK& K) {
+  const float m1 = __fmaf_rn(K.b1, m, __fmul_rn(K.omb1, g));
+  const float v1 = __fmaf_rn(K.b2, v, __fmul_rn(__fmul_rn(K.omb2, g), g));
+  const float den = __fmaf_rn(__fsqrt_rn(v1), K.rsbc2, K.eps);
+  th = __fsub_rn(th, __fdiv_rn(__fmul_rn(K.step, m1), den));
+  m = m1;
+  v = v1;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+__device__ __forceinline__ uint16_t bf16_rn(float x) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t*>(&b);
+}
+
+// ---------------------------------------------------------------- async copies and barriers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Gives up (returns
+// false) after timeout_ns of wall time, or at once when *abort is set.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                                  volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// Global -> shared bulk copy completing on an mbarrier (16-byte aligned, size multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Shared -> global bulk copy in the current bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void record_error(dp_step_state_t* st, int code) {
+  atomicCAS(&st->error, 0, code);
+}
+
+// End of a reduction kernel, run by thread 0 of every CTA: fold the CTA's
+// non-finite count into the state; the last CTA to arrive publishes
+// found_inf / nonfinite, optionally advances t and the beta powers, and
+// clears the work fields for the next call.
+__device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned long long cta_count, int cta_found,
+                                                 int advance, double b1, double b2) {
+  if (cta_count) atomicAdd(reinterpret_cast<unsigned long long*>(&st->work_count), cta_count);
+  if (cta_found) atomicOr(&st->work_found, 1u);
+  __threadfence();
+  const unsigned ticket = atomicAdd(&st->work_ticket, 1u);
+  if (ticket == gridDim.x - 1) {
+    __threadfence();
+    const unsigned f = atomicExch(&st->work_found, 0u);
+    const unsigned long long c = atomicExch(reinterpret_cast<unsigned long long*>(&st->work_count), 0ull);
+    const int err = *reinterpret_cast<volatile int*>(&st->error);
+    const int found = (f != 0u || err != 0) ? 1 : 0;
+    st->found_inf = found;
+    st->nonfinite = c;
+    if (advance && !found) {
+      st->t += 1;
+      st->b1t *= b1;
+      st->b2t *= b2;
+    }
+    __threadfence();
+    atomicExch(&st->work_ticket, 0u);
+  }
+}
+
+}  // namespace dp

@@ -1,0 +1,47 @@
+// Interface between the C ABI (dp_api.cu) and the kernel launchers (dp_kernels.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dpstep.h"
+
+namespace dp {
+
+struct PlanSeg {
+  int64_t goff, loff;
+  int32_t tile0, owner;
+};
+
+// A validated layout, empty segments dropped, tiles counted.
+struct Plan {
+  int32_t n, stage, nseg, ntiles;
+  int64_t psi;
+  int64_t shard_len[DP_MAX_N];
+  PlanSeg e[DP_MAX_SEG + 1];  // e[nseg] = {psi, 0, ntiles, 0}
+};
+
+struct StepScalars {
+  float lr, beta1, beta2, eps, omb1, omb2;
+  float inv;  // fl32(1 / (n S))
+  int32_t mode;
+  uint64_t timeout_ns;
+};
+
+// Each launcher returns the launch's cudaError_t and adds to *launches.
+cudaError_t launch_reduce(const Plan& P, const uint16_t* const* g, int a, float* const* gbar, const StepScalars& s,
+                          int advance, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_update(const Plan& P, uint16_t* const* rep, float* const* master, float* const* m,
+                          float* const* v, const float* const* gbar, const StepScalars& s,
+                          const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_accumulate(float* const* acc, const uint16_t* const* g, int64_t psi, int n, int first, int mode,
+                              cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_rs_avg(const Plan& P, const float* const* acc, float* const* gbar, const StepScalars& s,
+                          dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_advance(dp_step_state_t* st, double b1, double b2, cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_allgather(const Plan& P, uint16_t* const* rep, const float* const* master,
+                             const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_state_init(dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_selftest_wait(dp_step_state_t* st, uint64_t timeout_ns, cudaStream_t stream, uint64_t* launches);
+
+}  // namespace dp

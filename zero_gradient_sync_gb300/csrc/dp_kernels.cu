@@ -1,0 +1,773 @@
+// Kernels of the fused data-parallel step and their launchers (sm_103a).
+//
+// reduce (fused pass A): the n*a bf16 micro-step gradients of a tile are
+//   streamed once from HBM into a ring of shared-memory stages by one
+//   producer thread issuing 1-D bulk copies (cp.async.bulk, mbarrier
+//   transaction counts); 16 consumer warps fold each stage into per-element
+//   accumulators in the fixed order (micro-steps of a rank, then ranks in
+//   ring order s+1..s), scale by fl32(1/(n S)), count non-finite results and
+//   write gbar to the owner's shard.  The last CTA publishes the step's
+//   skip flag and advances t.
+// update (fused pass B): unless skipped, Adam on the fp32 master/m/v shard
+//   (16-byte vector loads/stores in local index space) and the bf16 image of
+//   the new master staged in shared memory, then bulk-stored into all n
+//   replicas (cp.async.bulk shared->global) at global index.
+// Staged kernels (accumulate, rs_avg, adam = update without replicas,
+//   allgather, advance) compute bit-identical results one phase at a time.
+#include <algorithm>
+
+#include "dp_device.cuh"
+#include "dp_internal.h"
+
+namespace dp {
+
+// ============================================================================ reduce (pass A)
+
+constexpr int RA_CWARPS = 16;
+constexpr int RA_CTHREADS = RA_CWARPS * 32;    // consumer threads: 8 elements each
+constexpr int RA_THREADS = RA_CTHREADS + 32;   // + one producer warp
+constexpr int RA_STAGES = 16;
+constexpr int RA_STAGE_BYTES = TILE * 2;       // one tile of one bf16 input
+constexpr int RA_OUT_BYTES = 2 * TILE * 4;     // double-buffered fp32 output tile
+constexpr int RA_SMEM = RA_STAGES * RA_STAGE_BYTES + RA_OUT_BYTES + 2 * RA_STAGES * 8 + 32;
+static_assert(TILE == RA_CTHREADS * 8, "one 16-byte group of 8 bf16 per consumer thread");
+
+template <int MAXSEG>
+struct ReduceParams {
+  const uint16_t* g[DP_MAX_NA];
+  float* gbar[DP_MAX_N];
+  dp_step_state_t* state;
+  uint64_t timeout_ns;
+  double beta1, beta2;
+  float inv;
+  int32_t n, a, advance;
+  SegTable<MAXSEG> seg;
+};
+
+template <int MAXSEG, bool COMP>
+__global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceParams<MAXSEG> p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* stages = smem;
+  float* outbuf = reinterpret_cast<float*>(smem + RA_STAGES * RA_STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RA_STAGES * RA_STAGE_BYTES + RA_OUT_BYTES);
+  uint64_t* empty = full + RA_STAGES;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + RA_STAGES);
+  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + RA_STAGES + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = p.n, a = p.a, na = n * a;
+  const int ntiles = p.seg.ntiles;
+  const int64_t psi = p.seg.psi;
+  const int64_t p8 = psi & ~int64_t(7);
+
+  if (tid == 0) {
+    for (int s = 0; s < RA_STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), RA_CWARPS);
+    }
+    *s_abort = 0;
+    *s_count = 0ull;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  unsigned bad = 0;
+  if (warp == RA_CWARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
+        const Tile t = tile_at(p.seg, tile);
+        const int64_t A = t.start & ~int64_t(7);
+        int64_t B = (t.end + 7) & ~int64_t(7);
+        if (B > p8) B = p8;
+        const uint32_t bytes = B > A ? (uint32_t)(B - A) * 2u : 0u;
+        int r = t.owner + 1 == n ? 0 : t.owner + 1;
+        int k = 0;
+        for (int q = 0; q < na; ++q, ++it) {
+          const uint32_t slot = it % RA_STAGES, use = it / RA_STAGES;
+          if (use > 0 && !mbar_wait_bounded(smem_u32(&empty[slot]), (use - 1) & 1u, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+            *s_abort = 1;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[slot]);
+          mbar_arrive_expect_tx(fb, bytes);
+          if (bytes) bulk_g2s(smem_u32(stages + slot * RA_STAGE_BYTES), p.g[r * a + k] + A, bytes, fb);
+          if (++k == a) {
+            k = 0;
+            if (++r == n) r = 0;
+          }
+        }
+      }
+      // Never leave with copies in flight: wait for the newest issued phase of every slot.
+      if (*s_abort) {
+        const uint32_t first = it > (uint32_t)RA_STAGES ? it - RA_STAGES : 0u;
+        for (uint32_t x = first; x < it; ++x)
+          (void)mbar_wait_bounded(smem_u32(&full[x % RA_STAGES]), (x / RA_STAGES) & 1u, p.timeout_ns, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumers
+    const f2_t inv2 = f2_pack(p.inv, p.inv);
+    uint32_t it = 0;
+    int buf = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, buf ^= 1) {
+      const Tile t = tile_at(p.seg, tile);
+      const int64_t A = t.start & ~int64_t(7);
+      const int64_t B = (t.end + 7) & ~int64_t(7);
+      const int64_t e0 = A + 8 * tid;
+      const bool active = e0 < B;
+      const bool tailgrp = active && (e0 + 8 > p8);
+      f2_t H[4], L[4], h[4], l[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) H[u] = L[u] = h[u] = l[u] = 0ull;
+      int r = t.owner + 1 == n ? 0 : t.owner + 1;
+      int j = 0, k = 0;
+      for (int q = 0; q < na; ++q, ++it) {
+        const uint32_t slot = it % RA_STAGES, par = (it / RA_STAGES) & 1u;
+        if (!*s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), par, p.timeout_ns, s_abort)) {
+          if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+          *s_abort = 1;
+        }
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (active && !*s_abort) {
+          if (!tailgrp) {
+            const uint4 v = *reinterpret_cast<const uint4*>(stages + slot * RA_STAGE_BYTES + 16 * tid);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+          } else {
+            // The last partial group of the buffer is read straight from global memory.
+            const uint16_t* src = p.g[r * a + k];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
+              w[u >> 1] |= (u & 1) ? (b << 16) : b;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const f2_t x = bf16x2_to_f2(w[u]);
+          if (COMP) {
+            if (k == 0) {
+              h[u] = x;
+              l[u] = 0ull;
+            } else {
+              f2_t e;
+              h[u] = f2_two_sum(h[u], x, e);
+              l[u] = f2_add(l[u], e);
+            }
+            if (k == a - 1) {
+              if (j == 0) {
+                H[u] = h[u];
+                L[u] = l[u];
+              } else {
+                f2_t e;
+                H[u] = f2_two_sum(H[u], h[u], e);
+                L[u] = f2_add(L[u], e);
+                L[u] = f2_add(L[u], l[u]);
+              }
+            }
+          } else {
+            h[u] = (k == 0) ? x : f2_add(h[u], x);
+            if (k == a - 1) H[u] = (j == 0) ? h[u] : f2_add(H[u], h[u]);
+          }
+        }
+        if (++k == a) {
+          k = 0;
+          ++j;
+          if (++r == n) r = 0;
+        }
+      }
+      // Finish the tile: gbar = fl(p * inv); count non-finite values of this tile's own elements.
+      float o[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const f2_t pp = COMP ? f2_add(H[u], L[u]) : H[u];
+        f2_unpack(f2_mul(pp, inv2), o[2 * u], o[2 * u + 1]);
+      }
+      float* ob = outbuf + buf * TILE;
+      if (active) {
+        float4* ob4 = reinterpret_cast<float4*>(ob + 8 * tid);
+        ob4[0] = make_float4(o[0], o[1], o[2], o[3]);
+        ob4[1] = make_float4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (e0 + u >= t.start && e0 + u < t.end && nonfinite(o[u])) ++bad;
+      }
+      named_bar_sync(1, RA_CTHREADS);
+      // Coalesced store into the owner's shard at local index (any alignment).
+      const int64_t cnt = t.end - t.start;
+      float* dst = p.gbar[t.owner] + t.loff + (t.start - t.goff);
+      const float* srcp = ob + (t.start - A);
+      for (int64_t x = tid; x < cnt; x += RA_CTHREADS) dst[x] = srcp[x];
+    }
+  }
+
+  // ------------------------------------------------------------ CTA total, then the grid's
+  unsigned long long c = bad;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+  __syncthreads();
+  if (lane == 0 && c) atomicAdd(s_count, c);
+  __syncthreads();
+  if (tid == 0) finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2);
+}
+
+// ============================================================================ update (pass B)
+
+constexpr int UB_THREADS = 256;
+constexpr int UB_GROUPS = TILE / 4 / UB_THREADS;  // 4-element groups per thread per tile
+static_assert(UB_GROUPS * 4 * UB_THREADS == TILE, "tile must split evenly");
+
+template <int MAXSEG>
+struct UpdateParams {
+  uint16_t* rep[DP_MAX_N];
+  float* master[DP_MAX_N];
+  float* m[DP_MAX_N];
+  float* v[DP_MAX_N];
+  const float* gbar[DP_MAX_N];
+  const dp_step_state_t* state;
+  float lr, beta1, beta2, eps, omb1, omb2;
+  int32_t n;
+  SegTable<MAXSEG> seg;
+};
+
+__device__ __forceinline__ bool update_prologue(const dp_step_state_t* st, float lr, AdamK& K, float* s_k) {
+  const volatile dp_step_state_t* vs = st;
+  if (vs->found_inf || vs->t == 0) return false;   // skipped step, or no reduction ran
+  if (threadIdx.x == 0) {
+    const double bc1 = 1.0 - vs->b1t, bc2 = 1.0 - vs->b2t;
+    s_k[0] = (float)((double)lr / bc1);
+    s_k[1] = (float)(1.0 / sqrt(bc2));
+  }
+  __syncthreads();
+  K.step = s_k[0];
+  K.rsbc2 = s_k[1];
+  return true;
+}
+
+__device__ __forceinline__ void stage_bf16x4(uint16_t* sb, int64_t off, uint32_t w0, uint32_t w1) {
+  if ((off & 3) == 0) {
+    *reinterpret_cast<uint2*>(sb + off) = make_uint2(w0, w1);
+  } else if ((off & 1) == 0) {
+    *reinterpret_cast<uint32_t*>(sb + off) = w0;
+    *reinterpret_cast<uint32_t*>(sb + off + 2) = w1;
+  } else {
+    sb[off] = (uint16_t)(w0 & 0xFFFFu);
+    sb[off + 1] = (uint16_t)(w0 >> 16);
+    sb[off + 2] = (uint16_t)(w1 & 0xFFFFu);
+    sb[off + 3] = (uint16_t)(w1 >> 16);
+  }
+}
+
+// Stages 1-3: shard arrays in local index space.  REPL: also all-gather.
+template <int MAXSEG, bool REPL>
+__global__ void __launch_bounds__(UB_THREADS) update_kernel(const __grid_constant__ UpdateParams<MAXSEG> p) {
+  __shared__ __align__(128) uint16_t sbuf[REPL ? 2 : 1][REPL ? TILE : 8];
+  __shared__ float s_k[2];
+  AdamK K;
+  K.b1 = p.beta1; K.b2 = p.beta2; K.omb1 = p.omb1; K.omb2 = p.omb2; K.eps = p.eps;
+  if (!update_prologue(p.state, p.lr, K, s_k)) return;
+  const int tid = threadIdx.x;
+  const int ntiles = p.seg.ntiles;
+  int it = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    const Tile t = tile_at(p.seg, tile);
+    const int64_t delta = t.loff - t.goff;
+    const int64_t js = t.start + delta, je = t.end + delta;
+    const int64_t jlo = (js + 3) & ~int64_t(3), jhi = je & ~int64_t(3);
+    const int ngr = jhi > jlo ? (int)((jhi - jlo) >> 2) : 0;
+    const int64_t cb = (t.start / TILE) * TILE;
+    float* __restrict__ M = p.master[t.owner];
+    float* __restrict__ Mm = p.m[t.owner];
+    float* __restrict__ Vv = p.v[t.owner];
+    const float* __restrict__ G = p.gbar[t.owner];
+    uint16_t* sb = sbuf[REPL ? (it & 1) : 0];
+    if (REPL) {
+      if (tid == 0) bulk_wait_read<1>();  // the bulk stores of two tiles ago have read this buffer
+      __syncthreads();
+    }
+    float4 g4[UB_GROUPS], t4[UB_GROUPS], m4[UB_GROUPS], v4[UB_GROUPS];
+#pragma unroll
+    for (int u = 0; u < UB_GROUPS; ++u) {
+      const int gq = tid + u * UB_THREADS;
+      if (gq < ngr) {
+        const int64_t jj = jlo + 4 * (int64_t)gq;
+        g4[u] = __ldcs(reinterpret_cast<const float4*>(G + jj));
+        t4[u] = *reinterpret_cast<const float4*>(M + jj);
+        m4[u] = *reinterpret_cast<const float4*>(Mm + jj);
+        v4[u] = *reinterpret_cast<const float4*>(Vv + jj);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UB_GROUPS; ++u) {
+      const int gq = tid + u * UB_THREADS;
+      if (gq < ngr) {
+        const int64_t jj = jlo + 4 * (int64_t)gq;
+        adam1(g4[u].x, t4[u].x, m4[u].x, v4[u].x, K);
+        adam1(g4[u].y, t4[u].y, m4[u].y, v4[u].y, K);
+        adam1(g4[u].z, t4[u].z, m4[u].z, v4[u].z, K);
+        adam1(g4[u].w, t4[u].w, m4[u].w, v4[u].w, K);
+        *reinterpret_cast<float4*>(M + jj) = t4[u];
+        *reinterpret_cast<float4*>(Mm + jj) = m4[u];
+        *reinterpret_cast<float4*>(Vv + jj) = v4[u];
+        if (REPL) stage_bf16x4(sb, jj - delta - cb, bf16x2_rn(t4[u].x, t4[u].y), bf16x2_rn(t4[u].z, t4[u].w));
+      }
+    }
+    // Ragged ends of the tile in local space (at most 3 elements each): scalar.
+    {
+      int64_t jx = -1;
+      if (tid < 4) {
+        jx = js + tid;
+        if (jx >= (jlo < je ? jlo : je)) jx = -1;
+      } else if (tid < 8) {
+        jx = (jhi > jlo ? jhi : jlo) + (tid - 4);
+        if (jx >= je) jx = -1;
+      }
+      if (jx >= 0) {
+        float th = M[jx], mm = Mm[jx], vv = Vv[jx];
+        adam1(G[jx], th, mm, vv, K);
+        M[jx] = th;
+        Mm[jx] = mm;
+        Vv[jx] = vv;
+        if (REPL) sb[jx - delta - cb] = bf16_rn(th);
+      }
+    }
+    if (REPL) {
+      fence_proxy_async_smem();
+      __syncthreads();
+      const int64_t ilo = (t.start + 7) & ~int64_t(7), ihi = t.end & ~int64_t(7);
+      if (tid == 0) {
+        if (ihi > ilo) {
+          const uint32_t src = smem_u32(sb + (ilo - cb));
+          const uint32_t bytes = (uint32_t)(ihi - ilo) * 2u;
+          for (int r = 0; r < p.n; ++r) bulk_s2g(p.rep[r] + ilo, src, bytes);
+        }
+        bulk_commit();
+      }
+      // Global-space ragged ends (fewer than 8 elements each) with plain stores.
+      if (tid < 16) {
+        int64_t ix = -1;
+        if (tid < 8) {
+          ix = t.start + tid;
+          if (ix >= (ilo < t.end ? ilo : t.end)) ix = -1;
+        } else {
+          ix = (ihi > ilo ? ihi : ilo) + (tid - 8);
+          if (ix >= t.end) ix = -1;
+        }
+        if (ix >= 0) {
+          const uint16_t b = sb[ix - cb];
+          for (int r = 0; r < p.n; ++r) p.rep[r][ix] = b;
+        }
+      }
+    }
+  }
+  if (REPL && tid == 0) bulk_wait_all();
+}
+
+// Stage 0 (plain data parallelism): every rank updates its own full-length
+// state with the owner's gbar, and writes its own replica.
+template <int MAXSEG, bool REPL>
+__global__ void __launch_bounds__(UB_THREADS) update_dp_kernel(const __grid_constant__ UpdateParams<MAXSEG> p) {
+  __shared__ float s_k[2];
+  AdamK K;
+  K.b1 = p.beta1; K.b2 = p.beta2; K.omb1 = p.omb1; K.omb2 = p.omb2; K.eps = p.eps;
+  if (!update_prologue(p.state, p.lr, K, s_k)) return;
+  const int ntiles = p.seg.ntiles;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const Tile t = tile_at(p.seg, tile);
+    const float* G = p.gbar[t.owner];
+    for (int64_t e = t.start + threadIdx.x; e < t.end; e += UB_THREADS) {
+      const float g = G[t.loff + (e - t.goff)];
+      for (int r = 0; r < p.n; ++r) {
+        float th = p.master[r][e], mm = p.m[r][e], vv = p.v[r][e];
+        adam1(g, th, mm, vv, K);
+        p.master[r][e] = th;
+        p.m[r][e] = mm;
+        p.v[r][e] = vv;
+        if (REPL) p.rep[r][e] = bf16_rn(th);
+      }
+    }
+  }
+}
+
+// ============================================================================ staged kernels
+
+struct AccParams {
+  float* acc[DP_MAX_N];
+  const uint16_t* g[DP_MAX_N];
+  int64_t psi;
+  int32_t n, first;
+};
+
+template <bool COMP>
+__global__ void __launch_bounds__(256) accumulate_kernel(const __grid_constant__ AccParams p) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < p.psi; e += stride) {
+    for (int r = 0; r < p.n; ++r) {
+      const float x = bf16_to_f32(p.g[r][e]);
+      if (COMP) {
+        float2* a2 = reinterpret_cast<float2*>(p.acc[r]) + e;
+        if (p.first) {
+          *a2 = make_float2(x, 0.0f);
+        } else {
+          float2 hl = *a2;
+          float err;
+          hl.x = two_sum(hl.x, x, err);
+          hl.y = __fadd_rn(hl.y, err);
+          *a2 = hl;
+        }
+      } else {
+        float* a1 = p.acc[r] + e;
+        *a1 = p.first ? x : __fadd_rn(*a1, x);
+      }
+    }
+  }
+}
+
+template <int MAXSEG>
+struct RsParams {
+  const float* acc[DP_MAX_N];
+  float* gbar[DP_MAX_N];
+  dp_step_state_t* state;
+  float inv;
+  int32_t n;
+  SegTable<MAXSEG> seg;
+};
+
+template <int MAXSEG, bool COMP>
+__global__ void __launch_bounds__(256) rs_avg_kernel(const __grid_constant__ RsParams<MAXSEG> p) {
+  __shared__ unsigned long long s_count;
+  if (threadIdx.x == 0) s_count = 0ull;
+  __syncthreads();
+  unsigned bad = 0;
+  const int n = p.n;
+  for (int tile = blockIdx.x; tile < p.seg.ntiles; tile += gridDim.x) {
+    const Tile t = tile_at(p.seg, tile);
+    float* dst = p.gbar[t.owner];
+    for (int64_t e = t.start + threadIdx.x; e < t.end; e += blockDim.x) {
+      int r = t.owner + 1 == n ? 0 : t.owner + 1;
+      float H = 0.0f, L = 0.0f;
+      for (int j = 0; j < n; ++j) {
+        if (COMP) {
+          const float2 hl = reinterpret_cast<const float2*>(p.acc[r])[e];
+          if (j == 0) {
+            H = hl.x;
+            L = hl.y;
+          } else {
+            float err;
+            H = two_sum(H, hl.x, err);
+            L = __fadd_rn(L, err);
+            L = __fadd_rn(L, hl.y);
+          }
+        } else {
+          const float h = p.acc[r][e];
+          H = (j == 0) ? h : __fadd_rn(H, h);
+        }
+        if (++r == n) r = 0;
+      }
+      const float pp = COMP ? __fadd_rn(H, L) : H;
+      const float g = __fmul_rn(pp, p.inv);
+      dst[t.loff + (e - t.goff)] = g;
+      if (nonfinite(g)) ++bad;
+    }
+  }
+  unsigned long long c = bad;
+  for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+  if ((threadIdx.x & 31) == 0 && c) atomicAdd(&s_count, c);
+  __syncthreads();
+  if (threadIdx.x == 0) finish_reduction(p.state, s_count, s_count != 0ull, 0, 1.0, 1.0);
+}
+
+template <int MAXSEG>
+struct AgParams {
+  uint16_t* rep[DP_MAX_N];
+  const float* master[DP_MAX_N];
+  const dp_step_state_t* state;
+  int32_t n, stage;
+  SegTable<MAXSEG> seg;
+};
+
+template <int MAXSEG>
+__global__ void __launch_bounds__(256) allgather_kernel(const __grid_constant__ AgParams<MAXSEG> p) {
+  const volatile dp_step_state_t* vs = p.state;
+  if (vs->found_inf) return;
+  for (int tile = blockIdx.x; tile < p.seg.ntiles; tile += gridDim.x) {
+    const Tile t = tile_at(p.seg, tile);
+    for (int64_t e = t.start + threadIdx.x; e < t.end; e += blockDim.x) {
+      if (p.stage == 0) {
+        for (int r = 0; r < p.n; ++r) p.rep[r][e] = bf16_rn(p.master[r][e]);
+      } else {
+        const uint16_t b = bf16_rn(p.master[t.owner][t.loff + (e - t.goff)]);
+        for (int r = 0; r < p.n; ++r) p.rep[r][e] = b;
+      }
+    }
+  }
+}
+
+__global__ void advance_kernel(dp_step_state_t* st, double b1, double b2) {
+  if (!st->found_inf) {
+    st->t += 1;
+    st->b1t *= b1;
+    st->b2t *= b2;
+  }
+}
+
+__global__ void state_init_kernel(dp_step_state_t* st) {
+  st->t = 0;
+  st->found_inf = 0;
+  st->error = 0;
+  st->reserved0 = 0;
+  st->nonfinite = 0ull;
+  st->b1t = 1.0;
+  st->b2t = 1.0;
+  st->work_count = 0ull;
+  st->work_found = 0u;
+  st->work_ticket = 0u;
+  st->reserved1 = 0ull;
+}
+
+// One block waits on a barrier that expects two arrivals but receives one.
+__global__ void selftest_wait_kernel(dp_step_state_t* st, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 2);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive(smem_u32(&bar));
+    if (!mbar_wait_bounded(smem_u32(&bar), 0u, timeout_ns, nullptr)) record_error(st, DP_ERR_TIMEOUT);
+  }
+}
+
+// ============================================================================ launchers
+
+static int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = v > 0 ? v : 148;
+  }
+  return cached[dev];
+}
+
+template <int MAXSEG>
+static void fill_seg(SegTable<MAXSEG>& T, const Plan& P) {
+  T.psi = P.psi;
+  T.nseg = P.nseg;
+  T.ntiles = P.ntiles;
+  for (int k = 0; k <= P.nseg; ++k) {
+    T.e[k].goff = P.e[k].goff;
+    T.e[k].loff = P.e[k].loff;
+    T.e[k].tile0 = P.e[k].tile0;
+    T.e[k].owner = P.e[k].owner;
+  }
+}
+
+template <typename K>
+static int occupancy_grid(K kernel, int threads, size_t smem, int ntiles) {
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  if (per_sm < 1) per_sm = 1;
+  long long g = (long long)sm_count() * per_sm;
+  if (ntiles < g) g = ntiles;
+  return (int)(g < 1 ? 1 : g);
+}
+
+template <int MAXSEG, bool COMP>
+static cudaError_t launch_reduce_t(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
+                                   const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream) {
+  ReduceParams<MAXSEG> prm;
+  for (int q = 0; q < P.n * a; ++q) prm.g[q] = g[q];
+  for (int r = 0; r < P.n; ++r) prm.gbar[r] = gbar[r];
+  prm.state = st;
+  prm.timeout_ns = s.timeout_ns;
+  prm.beta1 = (double)s.beta1;
+  prm.beta2 = (double)s.beta2;
+  prm.inv = s.inv;
+  prm.n = P.n;
+  prm.a = a;
+  prm.advance = advance;
+  fill_seg(prm.seg, P);
+  auto kern = reduce_kernel<MAXSEG, COMP>;
+  // The opt-in shared-memory size is set once per device (not inside a stream capture on later calls).
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RA_SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  // Every CTA takes part in the grid-wide finish, so at least one CTA runs even with no tiles.
+  int grid = sm_count();
+  if (P.ntiles < grid) grid = P.ntiles > 0 ? P.ntiles : 1;
+  kern<<<grid, RA_THREADS, RA_SMEM, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const Plan& P, const uint16_t* const* g, int a, float* const* gbar, const StepScalars& s,
+                          int advance, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  const bool comp = s.mode == DP_SUM_COMPENSATED;
+  if (P.nseg <= SMALL_SEG)
+    return comp ? launch_reduce_t<SMALL_SEG, true>(P, g, a, gbar, s, advance, st, stream)
+                : launch_reduce_t<SMALL_SEG, false>(P, g, a, gbar, s, advance, st, stream);
+  return comp ? launch_reduce_t<BIG_SEG, true>(P, g, a, gbar, s, advance, st, stream)
+              : launch_reduce_t<BIG_SEG, false>(P, g, a, gbar, s, advance, st, stream);
+}
+
+template <int MAXSEG>
+static cudaError_t launch_update_t(const Plan& P, uint16_t* const* rep, float* const* master, float* const* m,
+                                   float* const* v, const float* const* gbar, const StepScalars& s,
+                                   const dp_step_state_t* st, cudaStream_t stream) {
+  UpdateParams<MAXSEG> prm;
+  for (int r = 0; r < P.n; ++r) {
+    prm.rep[r] = rep ? rep[r] : nullptr;
+    prm.master[r] = master[r];
+    prm.m[r] = m[r];
+    prm.v[r] = v[r];
+    prm.gbar[r] = gbar[r];
+  }
+  prm.state = st;
+  prm.lr = s.lr;
+  prm.beta1 = s.beta1;
+  prm.beta2 = s.beta2;
+  prm.eps = s.eps;
+  prm.omb1 = s.omb1;
+  prm.omb2 = s.omb2;
+  prm.n = P.n;
+  fill_seg(prm.seg, P);
+  const int nt = P.ntiles > 0 ? P.ntiles : 1;
+  if (P.stage == 0) {
+    if (rep) {
+      auto k = update_dp_kernel<MAXSEG, true>;
+      k<<<occupancy_grid(k, UB_THREADS, 0, nt), UB_THREADS, 0, stream>>>(prm);
+    } else {
+      auto k = update_dp_kernel<MAXSEG, false>;
+      k<<<occupancy_grid(k, UB_THREADS, 0, nt), UB_THREADS, 0, stream>>>(prm);
+    }
+  } else {
+    if (rep) {
+      auto k = update_kernel<MAXSEG, true>;
+      k<<<occupancy_grid(k, UB_THREADS, 0, nt), UB_THREADS, 0, stream>>>(prm);
+    } else {
+      auto k = update_kernel<MAXSEG, false>;
+      k<<<occupancy_grid(k, UB_THREADS, 0, nt), UB_THREADS, 0, stream>>>(prm);
+    }
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_update(const Plan& P, uint16_t* const* rep, float* const* master, float* const* m,
+                          float* const* v, const float* const* gbar, const StepScalars& s,
+                          const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  if (P.nseg <= SMALL_SEG) return launch_update_t<SMALL_SEG>(P, rep, master, m, v, gbar, s, st, stream);
+  return launch_update_t<BIG_SEG>(P, rep, master, m, v, gbar, s, st, stream);
+}
+
+cudaError_t launch_accumulate(float* const* acc, const uint16_t* const* g, int64_t psi, int n, int first, int mode,
+                              cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  AccParams prm;
+  for (int r = 0; r < n; ++r) {
+    prm.acc[r] = acc[r];
+    prm.g[r] = g[r];
+  }
+  prm.psi = psi;
+  prm.n = n;
+  prm.first = first ? 1 : 0;
+  long long blocks = (psi + 255) / 256;
+  const long long cap = (long long)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (mode == DP_SUM_COMPENSATED)
+    accumulate_kernel<true><<<(int)blocks, 256, 0, stream>>>(prm);
+  else
+    accumulate_kernel<false><<<(int)blocks, 256, 0, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+template <int MAXSEG>
+static cudaError_t launch_rs_t(const Plan& P, const float* const* acc, float* const* gbar, const StepScalars& s,
+                               dp_step_state_t* st, cudaStream_t stream) {
+  RsParams<MAXSEG> prm;
+  for (int r = 0; r < P.n; ++r) {
+    prm.acc[r] = acc[r];
+    prm.gbar[r] = gbar[r];
+  }
+  prm.state = st;
+  prm.inv = s.inv;
+  prm.n = P.n;
+  fill_seg(prm.seg, P);
+  const int nt = P.ntiles > 0 ? P.ntiles : 1;
+  if (s.mode == DP_SUM_COMPENSATED) {
+    auto k = rs_avg_kernel<MAXSEG, true>;
+    k<<<occupancy_grid(k, 256, 0, nt), 256, 0, stream>>>(prm);
+  } else {
+    auto k = rs_avg_kernel<MAXSEG, false>;
+    k<<<occupancy_grid(k, 256, 0, nt), 256, 0, stream>>>(prm);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rs_avg(const Plan& P, const float* const* acc, float* const* gbar, const StepScalars& s,
+                          dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  if (P.nseg <= SMALL_SEG) return launch_rs_t<SMALL_SEG>(P, acc, gbar, s, st, stream);
+  return launch_rs_t<BIG_SEG>(P, acc, gbar, s, st, stream);
+}
+
+cudaError_t launch_advance(dp_step_state_t* st, double b1, double b2, cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  advance_kernel<<<1, 1, 0, stream>>>(st, b1, b2);
+  return cudaGetLastError();
+}
+
+template <int MAXSEG>
+static cudaError_t launch_ag_t(const Plan& P, uint16_t* const* rep, const float* const* master,
+                               const dp_step_state_t* st, cudaStream_t stream) {
+  AgParams<MAXSEG> prm;
+  for (int r = 0; r < P.n; ++r) {
+    prm.rep[r] = rep[r];
+    prm.master[r] = master[r];
+  }
+  prm.state = st;
+  prm.n = P.n;
+  prm.stage = P.stage;
+  fill_seg(prm.seg, P);
+  auto k = allgather_kernel<MAXSEG>;
+  k<<<occupancy_grid(k, 256, 0, P.ntiles > 0 ? P.ntiles : 1), 256, 0, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_allgather(const Plan& P, uint16_t* const* rep, const float* const* master,
+                             const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  if (P.nseg <= SMALL_SEG) return launch_ag_t<SMALL_SEG>(P, rep, master, st, stream);
+  return launch_ag_t<BIG_SEG>(P, rep, master, st, stream);
+}
+
+cudaError_t launch_state_init(dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  state_init_kernel<<<1, 1, 0, stream>>>(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(dp_step_state_t* st, uint64_t timeout_ns, cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(st, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace dp
