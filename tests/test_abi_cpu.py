@@ -16,8 +16,12 @@ HEADER = os.path.join(ROOT, "include", "dpstep.h")
 
 @pytest.fixture(scope="module")
 def dp():
-    from zero_gradient_sync_gb300 import build
-    build.build()
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_dpstep_build", os.path.join(ROOT, "zero_gradient_sync_gb300", "build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    b.build()
     import zero_gradient_sync_gb300 as z
     return z
 

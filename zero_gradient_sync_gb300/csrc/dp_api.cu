@@ -41,9 +41,11 @@ struct LaunchCount {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-dp_status_t check_ptr_array(const void* const* arr, int count, const char* name) {
+// lens (optional): elements behind each pointer; a pointer to zero elements may be NULL.
+dp_status_t check_ptr_array(const void* const* arr, int count, const char* name, const int64_t* lens = nullptr) {
   if (!arr) return fail(DP_ERR_INVALID_ARG, "%s: pointer array is NULL", name);
   for (int i = 0; i < count; ++i) {
+    if (!arr[i] && lens && lens[i] == 0) continue;
     if (!arr[i]) return fail(DP_ERR_INVALID_ARG, "%s[%d] is NULL", name, i);
     if (!aligned16(arr[i])) return fail(DP_ERR_ALIGNMENT, "%s[%d] is not 16-byte aligned", name, i);
   }
@@ -160,7 +162,7 @@ size_t align256(size_t x) { return (x + 255u) & ~size_t(255u); }
 dp_status_t gbar_ptrs(const Plan& P, float* const* gbar_shard, void* ws, float** out) {
   if (gbar_shard) {
     for (int r = 0; r < P.n; ++r) out[r] = gbar_shard[r];
-    return check_ptr_array((const void* const*)out, P.n, "gbar_shard");
+    return check_ptr_array((const void* const*)out, P.n, "gbar_shard", P.shard_len);
   }
   if (!ws) return fail(DP_ERR_INVALID_ARG, "both gbar_shard and ws are NULL");
   if (((uintptr_t)ws & 255u) != 0) return fail(DP_ERR_ALIGNMENT, "ws is not 256-byte aligned");
@@ -170,6 +172,26 @@ dp_status_t gbar_ptrs(const Plan& P, float* const* gbar_shard, void* ws, float**
     off += align256((size_t)P.shard_len[r] * sizeof(float));
   }
   return DP_OK;
+}
+
+// Lengths of each rank's master/m/v arrays: its shard, or psi for plain data parallelism.
+void state_lens(const Plan& P, int64_t* lens) {
+  for (int r = 0; r < P.n; ++r) lens[r] = P.stage == 0 ? P.psi : P.shard_len[r];
+}
+
+dp_status_t check_state_arrays(const Plan& P, float* const* master, float* const* m, float* const* v) {
+  int64_t lens[DP_MAX_N];
+  state_lens(P, lens);
+  dp_status_t st = check_ptr_array((const void* const*)master, P.n, "master", lens);
+  if (st == DP_OK) st = check_ptr_array((const void* const*)m, P.n, "m", lens);
+  if (st == DP_OK) st = check_ptr_array((const void* const*)v, P.n, "v", lens);
+  return st;
+}
+
+dp_status_t check_full_arrays(const Plan& P, const void* const* arr, int count, const char* name) {
+  int64_t lens[DP_MAX_NA];
+  for (int i = 0; i < count; ++i) lens[i] = P.psi;
+  return check_ptr_array(arr, count, name, lens);
 }
 
 }  // namespace
@@ -330,20 +352,14 @@ dp_status_t dp_reduce_scatter_avg(float* const* gbar_shard, const float* const* 
   if (st != DP_OK) return st;
   StepScalars s;
   if ((st = scalars(P, nullptr, loss_scale, sum_mode, s)) != DP_OK) return st;
-  if ((st = check_ptr_array((const void* const*)gbar_shard, P.n, "gbar_shard")) != DP_OK) return st;
-  if ((st = check_ptr_array((const void* const*)acc, P.n, "acc")) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)gbar_shard, P.n, "gbar_shard", P.shard_len)) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)acc, P.n, "acc")) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
   cudaError_t e = dp::launch_rs_avg(P, acc, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "reduce_scatter_avg launch");
 }
 
-static dp_status_t check_state_arrays(const Plan& P, float* const* master, float* const* m, float* const* v) {
-  dp_status_t st = check_ptr_array((const void* const*)master, P.n, "master");
-  if (st == DP_OK) st = check_ptr_array((const void* const*)m, P.n, "m");
-  if (st == DP_OK) st = check_ptr_array((const void* const*)v, P.n, "v");
-  return st;
-}
 
 dp_status_t dp_adam_shard(float* const* master, float* const* m, float* const* v, const float* const* gbar_shard,
                           const dp_layout_t* layout, dp_adam_t adam, dp_step_state_t* d_state, dp_stream_t stream) {
@@ -353,7 +369,7 @@ dp_status_t dp_adam_shard(float* const* master, float* const* m, float* const* v
   StepScalars s;
   if ((st = scalars(P, &adam, 1.0f, DP_SUM_COMPENSATED, s)) != DP_OK) return st;
   if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
-  if ((st = check_ptr_array((const void* const*)gbar_shard, P.n, "gbar_shard")) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)gbar_shard, P.n, "gbar_shard", P.shard_len)) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
   cudaError_t e = dp::launch_advance(d_state, (double)adam.beta1, (double)adam.beta2, (cudaStream_t)stream, &lc.n);
@@ -367,8 +383,12 @@ dp_status_t dp_allgather_params(uint16_t* const* replicas, const float* const* m
   static thread_local Plan P;
   dp_status_t st = build_plan(layout, P);
   if (st != DP_OK) return st;
-  if ((st = check_ptr_array((const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
-  if ((st = check_ptr_array((const void* const*)master, P.n, "master")) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  {
+    int64_t lens[DP_MAX_N];
+    state_lens(P, lens);
+    if ((st = check_ptr_array((const void* const*)master, P.n, "master", lens)) != DP_OK) return st;
+  }
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
   cudaError_t e = dp::launch_allgather(P, replicas, master, d_state, (cudaStream_t)stream, &lc.n);
@@ -381,7 +401,7 @@ static dp_status_t prepare_reduce(const Plan& P, const uint16_t* const* grads, i
   if (a < 1 || (int64_t)a * P.n > DP_MAX_NA)
     return fail(DP_ERR_INVALID_ARG, "a = %d: need 1 <= a and n * a <= %d", a, DP_MAX_NA);
   dp_status_t st = scalars(P, &adam, loss_scale, sum_mode, s);
-  if (st == DP_OK) st = check_ptr_array((const void* const*)grads, P.n * a, "grads");
+  if (st == DP_OK) st = check_full_arrays(P, (const void* const*)grads, P.n * a, "grads");
   if (st == DP_OK) st = gbar_ptrs(P, gbar_shard, ws, gb);
   if (st == DP_OK) st = check_state(d_state);
   return st;
@@ -411,7 +431,7 @@ dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, floa
   StepScalars s;
   if ((st = scalars(P, &adam, 1.0f, DP_SUM_COMPENSATED, s)) != DP_OK) return st;
   if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
-  if ((st = check_ptr_array((const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
   float* gb[DP_MAX_N];
   if ((st = gbar_ptrs(P, (float* const*)gbar_shard, ws, gb)) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
@@ -432,7 +452,7 @@ dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* cons
   if ((st = prepare_reduce(P, grads, a, adam, loss_scale, sum_mode, gbar_shard, ws, d_state, s, gb)) != DP_OK)
     return st;
   if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
-  if ((st = check_ptr_array((const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
   LaunchCount lc;
   cudaError_t e = dp::launch_reduce(P, grads, a, gb, s, 1, d_state, (cudaStream_t)stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
