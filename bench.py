@@ -43,6 +43,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=1 << 21, help="elements of the oracle's CPU sample")
+    p.add_argument("--psi", type=int, default=0, help="override the parameter count (small profiling cases)")
     return p.parse_args()
 
 
@@ -403,6 +404,8 @@ def main():
     if args.workload not in synth.WORKLOADS:
         raise SystemExit("unknown workload %s (have %s)" % (args.workload, ", ".join(synth.WORKLOADS)))
     wl = synth.WORKLOADS[args.workload]
+    if args.psi > 0:
+        wl = wl.with_(psi=args.psi, description=wl.description + " [psi overridden to %d]" % args.psi)
     if args.impl == "reference":
         return reference_main(args, wl)
     return native_main(args, wl)
