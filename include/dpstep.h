@@ -273,6 +273,30 @@ dp_status_t dp_read_status(const dp_step_state_t* d_state, int32_t* skipped, int
  * d_state->error and returns, leaving the context usable. */
 dp_status_t dp_selftest_wait_timeout(dp_step_state_t* d_state, uint64_t timeout_ns, dp_stream_t stream);
 
+/* ---- allocation-free variant ------------------------------------------------ */
+
+/* Size of the scratch array compiled into the library for dp_step_static. */
+#define DP_STATIC_SCRATCH_BYTES (64ll * 1024 * 1024)
+
+/* dp_step without caller-provided scratch.  The distributed-training pages
+ * have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory themselves -- a plugin inside a runtime that owns
+ * and pre-plans all device memory, a loop that must not allocate after
+ * start-up, or code running while another allocator holds a lock.
+ * The averaged-gradient shards live in a fixed 64 MiB array inside the
+ * library (DP_STATIC_SCRATCH_BYTES, held on every GPU that loads the library
+ * until the process exits): the layout's dp_workspace_size must not exceed
+ * it (about 16 million parameters), else DP_ERR_INVALID_ARG and nothing is
+ * launched.  Arguments, results and errors are those of dp_step; no call
+ * allocates or frees memory.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) -- make it before any stream
+ * capture on that device.  All calls share the array and it keeps the last
+ * call's contents; calls whose kernels overlap on the GPU race on it, so
+ * order them (one stream, or events). */
+dp_status_t dp_step_static(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                           const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                           float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

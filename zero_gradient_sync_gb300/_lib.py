@@ -77,6 +77,8 @@ def _load() -> ctypes.CDLL:
         "dp_step_update": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, P(dp_layout_t), dp_adam_t, c_vp, c_vp]),
         "dp_read_status": (c_i32, [c_vp, P(c_i32), P(c_i32), c_vp]),
         "dp_selftest_wait_timeout": (c_i32, [c_vp, c_u64, c_vp]),
+        "dp_step_static": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32,
+                                   c_vp, c_vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -261,6 +263,23 @@ def dp_step_update(replicas, master, m, v, gbar_shard, ws, layout: Layout, adam_
     gb, w = _gbar_args(layout, gbar_shard, ws)
     _check(LIB.dp_step_update(_ptr_array(replicas), _ptr_array(master), _ptr_array(m), _ptr_array(v), gb, w,
                               ctypes.byref(layout.c), adam_, _ptr(state), _stream(stream)), "dp_step_update")
+
+
+STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def dp_step_static(replicas, master, m, v, grads, a: int, layout: Layout, adam_: dp_adam_t, loss_scale: float,
+                   sum_mode: int = DP_SUM_COMPENSATED, state=None, stream=None) -> None:
+    """dp_step with its gradient-shard scratch inside the library (for callers that cannot allocate device
+    memory); the layout's workspace must fit STATIC_SCRATCH_BYTES."""
+    lens = layout.state_lens()
+    for name, ts in (("master", master), ("m", m), ("v", v)):
+        _check_tensors(ts, 4, lens, name)
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    _check_tensors(grads, 2, [layout.psi] * len(grads), "grads")
+    _check(LIB.dp_step_static(_ptr_array(replicas), _ptr_array(master), _ptr_array(m), _ptr_array(v),
+                              _ptr_array(grads), a, ctypes.byref(layout.c), adam_, loss_scale, sum_mode,
+                              _ptr(state), _stream(stream)), "dp_step_static")
 
 
 def dp_read_status(state, stream=None) -> Tuple[int, int]:

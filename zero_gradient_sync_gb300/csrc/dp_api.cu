@@ -196,6 +196,8 @@ dp_status_t check_full_arrays(const Plan& P, const void* const* arr, int count, 
 
 }  // namespace
 
+dp_status_t dp::report_error(dp_status_t s, const char* msg) { return fail(s, "%s", msg); }
+
 extern "C" {
 
 int32_t dp_abi_version(void) { return 1; }

@@ -28,6 +28,9 @@ struct StepScalars {
   uint64_t timeout_ns;
 };
 
+// Records msg as this thread's dp_last_error() and returns s.
+dp_status_t report_error(dp_status_t s, const char* msg);
+
 // Each launcher returns the launch's cudaError_t and adds to *launches.
 cudaError_t launch_reduce(const Plan& P, const uint16_t* const* g, int a, float* const* gbar, const StepScalars& s,
                           int advance, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
