@@ -15,7 +15,7 @@
 
 namespace dp {
 
-constexpr int TILE = 4096;          // elements per tile, multiple of 8
+constexpr int TILE = 7680;          // elements per tile, multiple of 8 (15 KB of bf16: one bulk copy)
 constexpr int SMALL_SEG = 32;       // segment-table capacity of the small kernel variants
 constexpr int BIG_SEG = DP_MAX_SEG; // ... and of the large ones
 
@@ -60,6 +60,25 @@ __device__ __forceinline__ Tile tile_at(const SegTable<MAXSEG>& T, int tile) {
   return t;
 }
 
+// Tiles of one CTA are visited in increasing order, so their segments are found by walking forward.
+template <int MAXSEG>
+struct TileWalker {
+  int seg = 0;
+  __device__ __forceinline__ Tile at(const SegTable<MAXSEG>& T, int tile) {
+    while (seg + 1 < T.nseg && T.e[seg + 1].tile0 <= tile) ++seg;
+    const int64_t goff = T.e[seg].goff;
+    const int64_t gend = T.e[seg + 1].goff;
+    const int64_t cell = goff / TILE + (tile - T.e[seg].tile0);
+    Tile t;
+    t.goff = goff;
+    t.loff = T.e[seg].loff;
+    t.owner = T.e[seg].owner;
+    t.start = goff > cell * TILE ? goff : cell * TILE;
+    t.end = gend < (cell + 1) * TILE ? gend : (cell + 1) * TILE;
+    return t;
+  }
+};
+
 // ---------------------------------------------------------------- fp32 arithmetic
 
 __device__ __forceinline__ bool nonfinite(float x) {
@@ -70,11 +89,16 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-// Knuth's TwoSum (TAOCP vol. 2, 4.2.2): s = fl(a + b) and e with s + e = a + b exactly.
+// Error-free sum: s = fl(a + b) and e with s + e = a + b exactly.  Computed as Dekker's Fast2Sum
+// (Numer. Math. 18, 1971) after ordering the operands by magnitude: s = big + small, e = small - (s - big).
+// For finite inputs (s, e) is unique, so this equals Knuth's TwoSum (TAOCP vol. 2, 4.2.2) except possibly
+// for the sign of a zero e, which the accumulators below cannot observe (their running error terms are
+// never -0: in round-to-nearest an exact zero sum is +0 unless both addends are -0).
 __device__ __forceinline__ float two_sum(float a, float b, float& e) {
-  const float s = __fadd_rn(a, b);
-  const float z = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+  const bool ge = fabsf(a) >= fabsf(b);
+  const float big = ge ? a : b, small = ge ? b : a;
+  const float s = __fadd_rn(big, small);
+  e = __fsub_rn(small, __fsub_rn(s, big));
   return s;
 }
 
@@ -105,13 +129,22 @@ __device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+// two_sum on a packed pair: the magnitude ordering per lane, the three additions packed.
 __device__ __forceinline__ f2_t f2_two_sum(f2_t a, f2_t b, f2_t& e) {
-  const f2_t s = f2_add(a, b);
-  const f2_t z = f2_sub(s, a);
-  e = f2_add(f2_sub(a, f2_sub(s, z)), f2_sub(b, z));
+  float a0, a1, b0, b1;
+  f2_unpack(a, a0, a1);
+  f2_unpack(b, b0, b1);
+  const bool g0 = fabsf(a0) >= fabsf(b0), g1 = fabsf(a1) >= fabsf(b1);
+  const f2_t big = f2_pack(g0 ? a0 : b0, g1 ? a1 : b1);
+  const f2_t small = f2_pack(g0 ? b0 : a0, g1 ? b1 : a1);
+  const f2_t s = f2_add(big, small);
+  e = f2_sub(small, f2_sub(s, big));
   return s;
 }
-__device__ __forceinline__ f2_t bf16x2_to_f2(uint32_t w) { return f2_pack(bf16_lo(w), bf16_hi(w)); }
+// Two bf16 (low half = first element) widened to an fp32 pair, built directly as one 64-bit value.
+__device__ __forceinline__ f2_t bf16x2_to_f2(uint32_t w) {
+  return ((f2_t)(w & 0xFFFF0000u) << 32) | (f2_t)(w << 16);
+}
 
 // ---------------------------------------------------------------- Adam
 

@@ -23,14 +23,15 @@ namespace dp {
 
 // ============================================================================ reduce (pass A)
 
-constexpr int RA_CWARPS = 16;
-constexpr int RA_CTHREADS = RA_CWARPS * 32;    // consumer threads: 8 elements each
-constexpr int RA_THREADS = RA_CTHREADS + 32;   // + one producer warp
-constexpr int RA_STAGES = 16;
-constexpr int RA_STAGE_BYTES = TILE * 2;       // one tile of one bf16 input
-constexpr int RA_OUT_BYTES = 2 * TILE * 4;     // double-buffered fp32 output tile
-constexpr int RA_SMEM = RA_STAGES * RA_STAGE_BYTES + RA_OUT_BYTES + 2 * RA_STAGES * 8 + 32;
-static_assert(TILE == RA_CTHREADS * 8, "one 16-byte group of 8 bf16 per consumer thread");
+constexpr int RA_CWARPS = 15;
+constexpr int RA_CTHREADS = RA_CWARPS * 32;    // consumer threads
+constexpr int RA_EPT = 16;                     // elements per consumer thread: two 16-byte shared loads
+constexpr int RA_THREADS = RA_CTHREADS + 32;   // + one producer warp: 16 warps, 4 per SM sub-partition
+constexpr int RA_STAGES = 12;
+constexpr int RA_STAGE_BYTES = TILE * 2;       // one tile of one bf16 input: a 15 KB bulk copy
+constexpr int RA_SMEM = RA_STAGES * RA_STAGE_BYTES + 2 * RA_STAGES * 8 + 32;
+static_assert(TILE == RA_CTHREADS * RA_EPT, "one 16-element group per consumer thread");
+static_assert(RA_STAGE_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
 
 template <int MAXSEG>
 struct ReduceParams {
@@ -44,18 +45,29 @@ struct ReduceParams {
   SegTable<MAXSEG> seg;
 };
 
+// Ring-buffer position of a stage: slot and the parity of its current use.
+struct RingPos {
+  uint32_t slot = 0, phase = 0, count = 0;
+  __device__ __forceinline__ void next() {
+    ++count;
+    if (++slot == RA_STAGES) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 template <int MAXSEG, bool COMP>
 __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceParams<MAXSEG> p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
-  float* outbuf = reinterpret_cast<float*>(smem + RA_STAGES * RA_STAGE_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RA_STAGES * RA_STAGE_BYTES + RA_OUT_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RA_STAGES * RA_STAGE_BYTES);
   uint64_t* empty = full + RA_STAGES;
   volatile int* s_abort = reinterpret_cast<volatile int*>(empty + RA_STAGES);
   unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + RA_STAGES + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = p.n, a = p.a, na = n * a;
+  const int n = p.n, a = p.a;
   const int ntiles = p.seg.ntiles;
   const int64_t psi = p.seg.psi;
   const int64_t p8 = psi & ~int64_t(7);
@@ -73,35 +85,36 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
 
   unsigned bad = 0;
   if (warp == RA_CWARPS) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer: one thread issues every copy
     if (lane == 0) {
-      uint32_t it = 0;
+      RingPos rp;
+      TileWalker<MAXSEG> walk;
       for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
-        const Tile t = tile_at(p.seg, tile);
+        const Tile t = walk.at(p.seg, tile);
         const int64_t A = t.start & ~int64_t(7);
         int64_t B = (t.end + 7) & ~int64_t(7);
         if (B > p8) B = p8;
         const uint32_t bytes = B > A ? (uint32_t)(B - A) * 2u : 0u;
         int r = t.owner + 1 == n ? 0 : t.owner + 1;
-        int k = 0;
-        for (int q = 0; q < na; ++q, ++it) {
-          const uint32_t slot = it % RA_STAGES, use = it / RA_STAGES;
-          if (use > 0 && !mbar_wait_bounded(smem_u32(&empty[slot]), (use - 1) & 1u, p.timeout_ns, s_abort)) {
-            if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
-            *s_abort = 1;
-            break;
+        for (int j = 0; j < n && !*s_abort; ++j) {
+          for (int k = 0; k < a; ++k) {
+            if (rp.count >= (uint32_t)RA_STAGES &&
+                !mbar_wait_bounded(smem_u32(&empty[rp.slot]), rp.phase ^ 1u, p.timeout_ns, s_abort)) {
+              if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+              *s_abort = 1;
+              break;
+            }
+            const uint32_t fb = smem_u32(&full[rp.slot]);
+            mbar_arrive_expect_tx(fb, bytes);
+            if (bytes) bulk_g2s(smem_u32(stages + rp.slot * RA_STAGE_BYTES), p.g[r * a + k] + A, bytes, fb);
+            rp.next();
           }
-          const uint32_t fb = smem_u32(&full[slot]);
-          mbar_arrive_expect_tx(fb, bytes);
-          if (bytes) bulk_g2s(smem_u32(stages + slot * RA_STAGE_BYTES), p.g[r * a + k] + A, bytes, fb);
-          if (++k == a) {
-            k = 0;
-            if (++r == n) r = 0;
-          }
+          if (++r == n) r = 0;
         }
       }
       // Never leave with copies in flight: wait for the newest issued phase of every slot.
       if (*s_abort) {
+        const uint32_t it = rp.count;
         const uint32_t first = it > (uint32_t)RA_STAGES ? it - RA_STAGES : 0u;
         for (uint32_t x = first; x < it; ++x)
           (void)mbar_wait_bounded(smem_u32(&full[x % RA_STAGES]), (x / RA_STAGES) & 1u, p.timeout_ns, nullptr);
@@ -109,101 +122,127 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ consumers
+    // ------------------------------------------------------------ consumers: 16 elements per thread
     const f2_t inv2 = f2_pack(p.inv, p.inv);
-    uint32_t it = 0;
-    int buf = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, buf ^= 1) {
-      const Tile t = tile_at(p.seg, tile);
+    RingPos rp;
+    TileWalker<MAXSEG> walk;
+    bool live = true;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const Tile t = walk.at(p.seg, tile);
       const int64_t A = t.start & ~int64_t(7);
       const int64_t B = (t.end + 7) & ~int64_t(7);
-      const int64_t e0 = A + 8 * tid;
+      const int64_t e0 = A + RA_EPT * tid;
       const bool active = e0 < B;
-      const bool tailgrp = active && (e0 + 8 > p8);
-      f2_t H[4], L[4], h[4], l[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) H[u] = L[u] = h[u] = l[u] = 0ull;
-      int r = t.owner + 1 == n ? 0 : t.owner + 1;
-      int j = 0, k = 0;
-      for (int q = 0; q < na; ++q, ++it) {
-        const uint32_t slot = it % RA_STAGES, par = (it / RA_STAGES) & 1u;
-        if (!*s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), par, p.timeout_ns, s_abort)) {
+      const bool tailgrp = active && (e0 + RA_EPT > p8);
+
+      // One stage: wait for its bytes, take this thread's 16 values, release the slot.  The shared abort
+      // flag is only read inside a wait that did not succeed at once; `live` is this thread's view.
+      auto take = [&](const uint16_t* src, uint32_t (&w)[8]) {
+        if (live && !mbar_wait_bounded(smem_u32(&full[rp.slot]), rp.phase, p.timeout_ns, s_abort)) {
           if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
           *s_abort = 1;
+          live = false;
         }
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (active && !*s_abort) {
-          if (!tailgrp) {
-            const uint4 v = *reinterpret_cast<const uint4*>(stages + slot * RA_STAGE_BYTES + 16 * tid);
-            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-          } else {
-            // The last partial group of the buffer is read straight from global memory.
-            const uint16_t* src = p.g[r * a + k];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 8; ++u) w[u] = 0u;
+        if (active && live) {
+          if (!tailgrp) {
+            const unsigned char* sp = stages + rp.slot * RA_STAGE_BYTES + 2 * RA_EPT * tid;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(sp);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(sp + 16);
+            w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+            w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+          } else {
+            // The group holding the buffer's last partial 8 elements is read from global memory.
+#pragma unroll
+            for (int u = 0; u < RA_EPT; ++u) {
               const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
               w[u >> 1] |= (u & 1) ? (b << 16) : b;
             }
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+        if (lane == 0) mbar_arrive(smem_u32(&empty[rp.slot]));
+        rp.next();
+      };
+
+      f2_t H[8], L[8];
+      int r = t.owner + 1 == n ? 0 : t.owner + 1;
+      for (int j = 0; j < n; ++j) {
+        const uint16_t* const* gr = p.g + r * a;
+        f2_t h[8], l[8];
+        uint32_t w[8];
+        take(gr[0], w);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const f2_t x = bf16x2_to_f2(w[u]);
-          if (COMP) {
-            if (k == 0) {
-              h[u] = x;
-              l[u] = 0ull;
-            } else {
+        for (int u = 0; u < 8; ++u) {
+          h[u] = bf16x2_to_f2(w[u]);
+          l[u] = 0ull;
+        }
+        for (int k = 1; k < a; ++k) {
+          take(gr[k], w);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const f2_t x = bf16x2_to_f2(w[u]);
+            if (COMP) {
               f2_t e;
               h[u] = f2_two_sum(h[u], x, e);
               l[u] = f2_add(l[u], e);
+            } else {
+              h[u] = f2_add(h[u], x);
             }
-            if (k == a - 1) {
-              if (j == 0) {
-                H[u] = h[u];
-                L[u] = l[u];
-              } else {
-                f2_t e;
-                H[u] = f2_two_sum(H[u], h[u], e);
-                L[u] = f2_add(L[u], e);
-                L[u] = f2_add(L[u], l[u]);
-              }
-            }
-          } else {
-            h[u] = (k == 0) ? x : f2_add(h[u], x);
-            if (k == a - 1) H[u] = (j == 0) ? h[u] : f2_add(H[u], h[u]);
           }
         }
-        if (++k == a) {
-          k = 0;
-          ++j;
-          if (++r == n) r = 0;
-        }
-      }
-      // Finish the tile: gbar = fl(p * inv); count non-finite values of this tile's own elements.
-      float o[8];
+        if (j == 0) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 8; ++u) {
+            H[u] = h[u];
+            L[u] = l[u];
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (COMP) {
+              f2_t e;
+              H[u] = f2_two_sum(H[u], h[u], e);
+              L[u] = f2_add(L[u], e);
+              // With one micro-step l is +0 and L is never -0, so L + l == L: the add is skipped.
+              if (a > 1) L[u] = f2_add(L[u], l[u]);
+            } else {
+              H[u] = f2_add(H[u], h[u]);
+            }
+          }
+        }
+        if (++r == n) r = 0;
+      }
+
+      // gbar = fl(p * inv) for the 16 elements; count the non-finite ones of this tile.
+      float o[RA_EPT];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
         const f2_t pp = COMP ? f2_add(H[u], L[u]) : H[u];
         f2_unpack(f2_mul(pp, inv2), o[2 * u], o[2 * u + 1]);
       }
-      float* ob = outbuf + buf * TILE;
       if (active) {
-        float4* ob4 = reinterpret_cast<float4*>(ob + 8 * tid);
-        ob4[0] = make_float4(o[0], o[1], o[2], o[3]);
-        ob4[1] = make_float4(o[4], o[5], o[6], o[7]);
+        const bool whole = e0 >= t.start && e0 + RA_EPT <= t.end;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (e0 + u >= t.start && e0 + u < t.end && nonfinite(o[u])) ++bad;
+        for (int u = 0; u < RA_EPT; ++u)
+          if ((whole || (e0 + u >= t.start && e0 + u < t.end)) && nonfinite(o[u])) ++bad;
+        // Store into the owner's shard at local index, with the widest access the alignment allows.
+        float* dst = p.gbar[t.owner] + (t.loff - t.goff + e0);
+        const int mis = (int)((t.loff - t.goff + e0) & 3);
+        if (whole && mis == 0) {
+#pragma unroll
+          for (int u = 0; u < RA_EPT; u += 4)
+            *reinterpret_cast<float4*>(dst + u) = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+        } else if (whole && mis == 2) {
+#pragma unroll
+          for (int u = 0; u < RA_EPT; u += 2) *reinterpret_cast<float2*>(dst + u) = make_float2(o[u], o[u + 1]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < RA_EPT; ++u)
+            if (e0 + u >= t.start && e0 + u < t.end) dst[u] = o[u];
+        }
       }
-      named_bar_sync(1, RA_CTHREADS);
-      // Coalesced store into the owner's shard at local index (any alignment).
-      const int64_t cnt = t.end - t.start;
-      float* dst = p.gbar[t.owner] + t.loff + (t.start - t.goff);
-      const float* srcp = ob + (t.start - A);
-      for (int64_t x = tid; x < cnt; x += RA_CTHREADS) dst[x] = srcp[x];
     }
   }
 
@@ -219,9 +258,9 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
 
 // ============================================================================ update (pass B)
 
-constexpr int UB_THREADS = 256;
-constexpr int UB_GROUPS = TILE / 4 / UB_THREADS;  // 4-element groups per thread per tile
-static_assert(UB_GROUPS * 4 * UB_THREADS == TILE, "tile must split evenly");
+constexpr int UB_THREADS = 512;
+constexpr int UB_GROUPS = (TILE / 4 + UB_THREADS - 1) / UB_THREADS;  // 4-element groups per thread per tile
+static_assert(UB_GROUPS * 4 * UB_THREADS >= TILE + 4, "a tile's 4-groups (one extra when misaligned) fit");
 
 template <int MAXSEG>
 struct UpdateParams {
