@@ -161,6 +161,9 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
             }
           }
         }
+        // The slot is refilled by the async proxy (bulk copy): order this thread's generic-proxy reads of
+        // it before that write, then release the slot.
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[rp.slot]));
         rp.next();
