@@ -150,7 +150,7 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0):
         b.update(A)
         torch.cuda.synchronize()
         st2 = dp.read_state(b.state)
-        assert (st2["found_inf"], st2["nonfinite"], st2["t"]) == (1, 1, t0 + 1)
+        assert (st2["found_inf"], st2["nonfinite"], st2["t"]) == (1, 1, t0 + 1 + repeat)
         after = [gather_state(x, segs, idx, wl.stage) for x in (b.master, b.m, b.v)]
         for x, y in zip(before, after):
             assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
