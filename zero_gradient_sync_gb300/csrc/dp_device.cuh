@@ -129,8 +129,17 @@ __device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-// two_sum on a packed pair: the magnitude ordering per lane, the three additions packed.
+// Knuth's TwoSum on a packed pair: six packed additions, no ordering (FP32 pipes only).
 __device__ __forceinline__ f2_t f2_two_sum(f2_t a, f2_t b, f2_t& e) {
+  const f2_t s = f2_add(a, b);
+  const f2_t z = f2_sub(s, a);
+  e = f2_add(f2_sub(a, f2_sub(s, z)), f2_sub(b, z));
+  return s;
+}
+// The same error-free sum as Fast2Sum after per-lane magnitude ordering: three packed additions plus a
+// compare and two selects per lane (spreads the work over the integer pipe).  Same (s, e) as f2_two_sum
+// for finite inputs, up to the sign of a zero e.
+__device__ __forceinline__ f2_t f2_fast_two_sum(f2_t a, f2_t b, f2_t& e) {
   float a0, a1, b0, b1;
   f2_unpack(a, a0, a1);
   f2_unpack(b, b0, b1);

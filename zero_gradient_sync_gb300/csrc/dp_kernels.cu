@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
             const f2_t x = bf16x2_to_f2(w[u]);
             if (COMP) {
               f2_t e;
-              h[u] = f2_two_sum(h[u], x, e);
+              h[u] = f2_fast_two_sum(h[u], x, e);   // measured faster here; the rank combine uses TwoSum
               l[u] = f2_add(l[u], e);
             } else {
               h[u] = f2_add(h[u], x);
