@@ -54,6 +54,28 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (one all-reduce of 8 bytes); x itself when not distributed."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(psi: int, world_size: int, ms_per_step: float) -> float:
+    """Whole-job Gparams/s: every rank processes its own replica of psi parameters per step (weak scaling)."""
+    return psi * world_size / (ms_per_step * 1e-3) / 1e9
+
+
+def barrier() -> None:
+    import torch.distributed as tdist
+    if tdist.is_available() and tdist.is_initialized() and tdist.get_world_size() > 1:
+        tdist.barrier()
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -278,11 +300,6 @@ def native_main(args, wl):
         bufs.update(A)
     torch.cuda.synchronize()
 
-    def barrier():
-        if ws > 1:
-            import torch.distributed as tdist
-            tdist.barrier()
-
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     end = torch.cuda.Event(enable_timing=True)
@@ -310,14 +327,10 @@ def native_main(args, wl):
     upd_ms = [ev[k][1].elapsed_time(ev[k + 1][0] if k + 1 < K else end) for k in range(K)]
     clk = clocks.stop()
     skipped, err = bufs.status()
-    if ws > 1:
-        import torch.distributed as tdist
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms = total_ms / K
     psi_all = wl.psi * ws
-    value = psi_all / (ms * 1e-3) / 1e9
+    value = job_throughput(wl.psi, ws, ms)
 
     b1, b2, red_bytes, upd_bytes = step_bytes(wl)
     peak, peak_kind = measured_peak()
@@ -347,13 +360,8 @@ def native_main(args, wl):
         s1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e_ms = s0.elapsed_time(s1) / KE
-        if ws > 1:
-            import torch.distributed as tdist
-            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": psi_all / (e_ms * 1e-3) / 1e9, "unit": "Gparams/s",
+        e_ms = max_over_ranks(s0.elapsed_time(s1) / KE, dev)
+        e2e = {"value": job_throughput(wl.psi, ws, e_ms), "unit": "Gparams/s",
                "h2d_bytes_per_step": 2 * wl.n * wl.a * wl.psi, "d2h_bytes_per_step": dp.STATE_BYTES,
                "ms_per_step": e_ms, "steps": KE}
 
