@@ -120,15 +120,31 @@ typedef struct {
 typedef struct {
   int32_t t;          /* Adam steps applied so far */
   int32_t found_inf;  /* 1 if the last reduction found a non-finite value: the step was skipped */
-  int32_t error;      /* sticky device-side error (DP_ERR_TIMEOUT) or 0; a set error skips every step */
-  int32_t reserved0;
+  int32_t error;      /* sticky device-side error (DP_ERR_TIMEOUT, DP_ERR_INVALID_ARG for a bad device
+                         loss scale) or 0; a set error skips every step */
+  int32_t good_steps; /* dynamic loss scale: applied steps since the scale last changed */
   uint64_t nonfinite; /* elements whose reduced gradient was not finite, last reduction */
   double b1t, b2t;    /* beta1^t and beta2^t, running products */
   uint64_t work_count;  /* kernel-internal, zero between calls */
   uint32_t work_found;  /* kernel-internal, zero between calls */
   uint32_t work_ticket; /* kernel-internal, zero between calls */
-  uint64_t reserved1;
+  float loss_scale;   /* dynamic loss scale used by dp_step_scaled (set by dp_scaler_init) */
+  uint32_t reserved1;
 } dp_step_state_t;
+
+/* Dynamic loss-scale policy of dp_step_scaled.  After each reduction:
+ *   overflow (step skipped):  scale = max(scale * backoff_factor, min_scale), good_steps = 0
+ *   clean step:               good_steps += 1; when it reaches growth_interval,
+ *                             scale = min(scale * growth_factor, max_scale), good_steps = 0
+ * (the growth/back-off rule of common mixed-precision loss scalers, with the scale kept in
+ * [min_scale, max_scale]; the pages only name loss scaling as training state to keep and align). */
+typedef struct {
+  float growth_factor;    /* >= 1 */
+  float backoff_factor;   /* in (0, 1] */
+  int32_t growth_interval; /* >= 1 */
+  float min_scale;        /* > 0 */
+  float max_scale;        /* >= min_scale, finite */
+} dp_scaler_t;
 
 /* ---- host helpers (no GPU needed) --------------------------------------- */
 
@@ -263,6 +279,21 @@ dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* c
 dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
                            const float* const* gbar_shard, void* ws, const dp_layout_t* layout, dp_adam_t adam,
                            const dp_step_state_t* d_state, dp_stream_t stream);
+
+/* Sets the device-resident dynamic loss scale of *d_state to `scale` (> 0,
+ * finite) and good_steps to 0 (one kernel).  Other fields are untouched. */
+dp_status_t dp_scaler_init(dp_step_state_t* d_state, float scale, dp_stream_t stream);
+
+/* dp_step with a dynamic loss scale: the reduction unscales by the scale held
+ * in d_state->loss_scale (read on the device, so no host round trip), and the
+ * last CTA of the reduction updates that scale with `scaler` once the skip
+ * decision is known.  A scale that is not positive and finite, or whose
+ * 1 / (n S) is not a normal fp32 number, records DP_ERR_INVALID_ARG in
+ * d_state->error and the step is skipped.  Other arguments as dp_step. */
+dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                           const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                           const dp_scaler_t* scaler, int32_t sum_mode, float* const* gbar_shard, void* ws,
+                           dp_step_state_t* d_state, dp_stream_t stream);
 
 /* Reads found_inf and error of *d_state into host ints after synchronising
  * the stream (the one blocking call).  skipped / err may be NULL. */

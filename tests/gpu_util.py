@@ -29,7 +29,7 @@ def state_bytes(t: int, beta1: float, beta2: float) -> bytes:
     for _ in range(t):
         b1t *= float(np.float32(beta1))
         b2t *= float(np.float32(beta2))
-    return struct.pack("<iiiiQddQIIQ", t, 0, 0, 0, 0, b1t, b2t, 0, 0, 0, 0)
+    return struct.pack("<iiiiQddQIIfI", t, 0, 0, 0, 0, b1t, b2t, 0, 0, 0, 0.0, 0)
 
 
 @dataclass

@@ -52,7 +52,8 @@ def test_abi_struct_sizes(dp):
     assert ctypes.sizeof(_lib.dp_layout_t) == 32
     assert ctypes.sizeof(_lib.dp_adam_t) == 16
     assert ctypes.sizeof(_lib.dp_step_state_t) == 64
-    assert dp.LIB.dp_abi_version() == 1
+    assert dp.LIB.dp_abi_version() == 2
+    assert ctypes.sizeof(_lib.dp_scaler_t) == 20
 
 
 @pytest.mark.parametrize("psi,n,bucket,mis", [(0, 2, 0, 0), (7, 8, 0, 0), ((1 << 20) + 3, 8, 0, 0),

@@ -406,3 +406,33 @@ def test_ring_detects_lost_message():
     rg.drop = ("rs", 1, 2)
     with pytest.raises(RuntimeError, match="message lost"):
         rg.reduce_scatter([np.ones(psi, np.float32)] * n)
+
+
+# ---------------------------------------------------------------- dynamic loss scale
+
+def test_scaler_policy_matches_torch_amp_update():
+    """With no clamping, the oracle's scale policy equals torch's own loss-scale update (library)."""
+    torch = pytest.importorskip("torch")
+    from oracle import scaler
+    rng = np.random.default_rng(5)
+    for growth, backoff, interval in ((2.0, 0.5, 3), (2.0, 0.25, 1), (1.5, 0.5, 7)):
+        s_t = torch.tensor([2.0 ** 16])
+        g_t = torch.tensor([0], dtype=torch.int32)
+        f_t = torch.tensor([0.0])
+        s, g = 2.0 ** 16, 0
+        for step in range(200):
+            found = bool(rng.random() < 0.15)
+            f_t.fill_(1.0 if found else 0.0)
+            torch._amp_update_scale_(s_t, g_t, f_t, growth, backoff, interval)
+            s, g = scaler.update(s, g, found, growth, backoff, interval, 0.0, float(np.finfo(np.float32).max))
+            assert s == s_t.item() and g == g_t.item()
+
+
+def test_scaler_clamps_to_range():
+    from oracle import scaler
+    s, g = 2.0 ** 24, 0
+    s, g = scaler.update(s, 1, False, 2.0, 0.5, 2, 2.0 ** 8, 2.0 ** 24)
+    assert (s, g) == (2.0 ** 24, 0)
+    s, g = 2.0 ** 8, 0
+    s, g = scaler.update(s, g, True, 2.0, 0.5, 2, 2.0 ** 8, 2.0 ** 24)
+    assert (s, g) == (2.0 ** 8, 0)

@@ -36,9 +36,15 @@ class dp_adam_t(ctypes.Structure):
 
 
 class dp_step_state_t(ctypes.Structure):
-    _fields_ = [("t", c_i32), ("found_inf", c_i32), ("error", c_i32), ("reserved0", c_i32), ("nonfinite", c_u64),
+    _fields_ = [("t", c_i32), ("found_inf", c_i32), ("error", c_i32), ("good_steps", c_i32), ("nonfinite", c_u64),
                 ("b1t", ctypes.c_double), ("b2t", ctypes.c_double), ("work_count", c_u64),
-                ("work_found", ctypes.c_uint32), ("work_ticket", ctypes.c_uint32), ("reserved1", c_u64)]
+                ("work_found", ctypes.c_uint32), ("work_ticket", ctypes.c_uint32), ("loss_scale", c_f32),
+                ("reserved1", ctypes.c_uint32)]
+
+
+class dp_scaler_t(ctypes.Structure):
+    _fields_ = [("growth_factor", c_f32), ("backoff_factor", c_f32), ("growth_interval", c_i32),
+                ("min_scale", c_f32), ("max_scale", c_f32)]
 
 
 assert ctypes.sizeof(dp_step_state_t) == STATE_BYTES
@@ -77,6 +83,9 @@ def _load() -> ctypes.CDLL:
         "dp_step_update": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, P(dp_layout_t), dp_adam_t, c_vp, c_vp]),
         "dp_read_status": (c_i32, [c_vp, P(c_i32), P(c_i32), c_vp]),
         "dp_selftest_wait_timeout": (c_i32, [c_vp, c_u64, c_vp]),
+        "dp_scaler_init": (c_i32, [c_vp, c_f32, c_vp]),
+        "dp_step_scaled": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, P(dp_scaler_t), c_i32,
+                                   c_vp, c_vp, c_vp, c_vp]),
         "dp_step_static": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32,
                                    c_vp, c_vp]),
     }
@@ -282,6 +291,28 @@ def dp_step_static(replicas, master, m, v, grads, a: int, layout: Layout, adam_:
                               _ptr(state), _stream(stream)), "dp_step_static")
 
 
+def scaler(growth_factor: float = 2.0, backoff_factor: float = 0.5, growth_interval: int = 2000,
+           min_scale: float = 2.0 ** 8, max_scale: float = 2.0 ** 24) -> dp_scaler_t:
+    return dp_scaler_t(growth_factor, backoff_factor, growth_interval, min_scale, max_scale)
+
+
+def dp_scaler_init(state, scale: float, stream=None) -> None:
+    _check(LIB.dp_scaler_init(_ptr(state), scale, _stream(stream)), "dp_scaler_init")
+
+
+def dp_step_scaled(replicas, master, m, v, grads, a: int, layout: Layout, adam_: dp_adam_t, scaler_: dp_scaler_t,
+                   sum_mode: int = DP_SUM_COMPENSATED, gbar_shard=None, ws=None, state=None, stream=None) -> None:
+    lens = layout.state_lens()
+    for name, ts in (("master", master), ("m", m), ("v", v)):
+        _check_tensors(ts, 4, lens, name)
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    _check_tensors(grads, 2, [layout.psi] * len(grads), "grads")
+    gb, w = _gbar_args(layout, gbar_shard, ws)
+    _check(LIB.dp_step_scaled(_ptr_array(replicas), _ptr_array(master), _ptr_array(m), _ptr_array(v),
+                              _ptr_array(grads), a, ctypes.byref(layout.c), adam_, ctypes.byref(scaler_), sum_mode,
+                              gb, w, _ptr(state), _stream(stream)), "dp_step_scaled")
+
+
 def dp_read_status(state, stream=None) -> Tuple[int, int]:
     sk, er = c_i32(0), c_i32(0)
     _check(LIB.dp_read_status(_ptr(state), ctypes.byref(sk), ctypes.byref(er), _stream(stream)), "dp_read_status")
@@ -333,4 +364,5 @@ def read_state(state) -> dict:
     raw = bytes(state.detach().cpu().numpy().tobytes())
     s = dp_step_state_t.from_buffer_copy(raw)
     return {"t": s.t, "found_inf": s.found_inf, "error": s.error, "nonfinite": s.nonfinite, "b1t": s.b1t,
-            "b2t": s.b2t, "work_count": s.work_count, "work_found": s.work_found, "work_ticket": s.work_ticket}
+            "b2t": s.b2t, "work_count": s.work_count, "work_found": s.work_found, "work_ticket": s.work_ticket,
+            "good_steps": s.good_steps, "loss_scale": s.loss_scale}

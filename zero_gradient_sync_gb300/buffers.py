@@ -41,6 +41,11 @@ class StepBuffers:
         _lib.dp_step(self.replicas, self.master, self.m, self.v, self.grads, self.a, self.layout, adam_,
                      loss_scale, sum_mode, gbar_shard=self.gbar, state=self.state, stream=stream)
 
+    def step_scaled(self, adam_: _lib.dp_adam_t, scaler_: _lib.dp_scaler_t, sum_mode: int = DP_SUM_COMPENSATED,
+                    stream=None) -> None:
+        _lib.dp_step_scaled(self.replicas, self.master, self.m, self.v, self.grads, self.a, self.layout, adam_,
+                            scaler_, sum_mode, gbar_shard=self.gbar, state=self.state, stream=stream)
+
     def reduce(self, adam_: _lib.dp_adam_t, loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED,
                stream=None) -> None:
         _lib.dp_step_reduce(self.gbar, None, self.grads, self.a, self.layout, adam_, loss_scale, sum_mode,

@@ -141,6 +141,7 @@ dp_status_t scalars(const Plan& P, const dp_adam_t* A, float loss_scale, int sum
   s.inv = inv32;
   s.mode = sum_mode;
   s.timeout_ns = g_timeout_ns.load();
+  s.scaler = dp::ScalerK{0, 1, 1.0f, 1.0f, 1.0f, 1.0f};
   if (A) {
     dp_status_t st = check_adam(*A);
     if (st != DP_OK) return st;
@@ -200,7 +201,7 @@ dp_status_t dp::report_error(dp_status_t s, const char* msg) { return fail(s, "%
 
 extern "C" {
 
-int32_t dp_abi_version(void) { return 1; }
+int32_t dp_abi_version(void) { return 2; }
 
 const char* dp_status_str(dp_status_t s) {
   switch (s) {
@@ -455,6 +456,44 @@ dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* cons
     return st;
   if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
   if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_reduce(P, grads, a, gb, s, 1, d_state, (cudaStream_t)stream, &lc.n);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
+  e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
+}
+
+dp_status_t dp_scaler_init(dp_step_state_t* d_state, float scale, dp_stream_t stream) {
+  dp_status_t st = check_state(d_state);
+  if (st != DP_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(DP_ERR_INVALID_ARG, "scale must be finite and > 0");
+  LaunchCount lc;
+  cudaError_t e = dp::launch_scaler_init(d_state, scale, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "scaler_init launch");
+}
+
+dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                           const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                           const dp_scaler_t* scaler, int32_t sum_mode, float* const* gbar_shard, void* ws,
+                           dp_step_state_t* d_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  if (!scaler) return fail(DP_ERR_INVALID_ARG, "scaler is NULL");
+  const dp_scaler_t& c = *scaler;
+  if (!(std::isfinite(c.growth_factor) && c.growth_factor >= 1.0f) ||
+      !(c.backoff_factor > 0.0f && c.backoff_factor <= 1.0f) || c.growth_interval < 1 ||
+      !(c.min_scale > 0.0f) || !std::isfinite(c.max_scale) || !(c.max_scale >= c.min_scale))
+    return fail(DP_ERR_INVALID_ARG, "scaler: need growth >= 1, backoff in (0, 1], interval >= 1, "
+                                    "0 < min_scale <= max_scale < inf");
+  StepScalars s;
+  float* gb[DP_MAX_N];
+  // The fixed-scale checks run with scale 1; the real scale is read and checked on the device.
+  if ((st = prepare_reduce(P, grads, a, adam, 1.0f, sum_mode, gbar_shard, ws, d_state, s, gb)) != DP_OK)
+    return st;
+  if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  s.scaler = dp::ScalerK{1, c.growth_interval, c.growth_factor, c.backoff_factor, c.min_scale, c.max_scale};
   LaunchCount lc;
   cudaError_t e = dp::launch_reduce(P, grads, a, gb, s, 1, d_state, (cudaStream_t)stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");

@@ -260,8 +260,15 @@ __device__ __forceinline__ void record_error(dp_step_state_t* st, int code) {
 // non-finite count into the state; the last CTA to arrive publishes
 // found_inf / nonfinite, optionally advances t and the beta powers, and
 // clears the work fields for the next call.
+// Dynamic loss-scale policy applied by the last CTA of a reduction (see dp_scaler_t).
+struct ScalerK {
+  int32_t enabled, interval;
+  float growth, backoff, min_scale, max_scale;
+};
+
 __device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned long long cta_count, int cta_found,
-                                                 int advance, double b1, double b2) {
+                                                 int advance, double b1, double b2,
+                                                 const ScalerK* scaler = nullptr) {
   if (cta_count) atomicAdd(reinterpret_cast<unsigned long long*>(&st->work_count), cta_count);
   if (cta_found) atomicOr(&st->work_found, 1u);
   __threadfence();
@@ -278,6 +285,19 @@ __device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned l
       st->t += 1;
       st->b1t *= b1;
       st->b2t *= b2;
+    }
+    if (scaler && scaler->enabled && err == 0) {
+      float sc = st->loss_scale;
+      if (found) {
+        sc = fmaxf(__fmul_rn(sc, scaler->backoff), scaler->min_scale);
+        st->good_steps = 0;
+      } else if (st->good_steps + 1 >= scaler->interval) {
+        sc = fminf(__fmul_rn(sc, scaler->growth), scaler->max_scale);
+        st->good_steps = 0;
+      } else {
+        st->good_steps += 1;
+      }
+      st->loss_scale = sc;
     }
     __threadfence();
     atomicExch(&st->work_ticket, 0u);

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "dp_device.cuh"
 #include "dpstep.h"
 
 namespace dp {
@@ -26,6 +27,7 @@ struct StepScalars {
   float inv;  // fl32(1 / (n S))
   int32_t mode;
   uint64_t timeout_ns;
+  ScalerK scaler;  // disabled unless the step uses the device-resident loss scale
 };
 
 // Records msg as this thread's dp_last_error() and returns s.
@@ -45,6 +47,7 @@ cudaError_t launch_advance(dp_step_state_t* st, double b1, double b2, cudaStream
 cudaError_t launch_allgather(const Plan& P, uint16_t* const* rep, const float* const* master,
                              const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
 cudaError_t launch_state_init(dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_scaler_init(dp_step_state_t* st, float scale, cudaStream_t stream, uint64_t* launches);
 cudaError_t launch_selftest_wait(dp_step_state_t* st, uint64_t timeout_ns, cudaStream_t stream, uint64_t* launches);
 
 }  // namespace dp

@@ -42,6 +42,7 @@ struct ReduceParams {
   double beta1, beta2;
   float inv;
   int32_t n, a, advance;
+  ScalerK scaler;    // enabled: unscale by the device-resident scale, then update it
   SegTable<MAXSEG> seg;
 };
 
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
   uint64_t* empty = full + RA_STAGES;
   volatile int* s_abort = reinterpret_cast<volatile int*>(empty + RA_STAGES);
   unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + RA_STAGES + 1);
+  __shared__ float s_inv;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = p.n, a = p.a;
@@ -79,6 +81,18 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
     }
     *s_abort = 0;
     *s_count = 0ull;
+    float inv = p.inv;
+    if (p.scaler.enabled) {
+      // fl32(1 / (n S)) from the device-resident scale, as the host computes it for a fixed scale.
+      const float sc = *reinterpret_cast<volatile const float*>(&p.state->loss_scale);
+      inv = (float)(1.0 / ((double)p.n * (double)sc));
+      if (!(sc > 0.0f) || nonfinite(sc) || !(inv >= 1.17549435e-38f) || nonfinite(inv)) {
+        record_error(p.state, DP_ERR_INVALID_ARG);
+        *s_abort = 1;    // skip the work; the finish sees the error and skips the step
+        inv = 0.0f;
+      }
+    }
+    s_inv = inv;
     fence_mbar_init();
   }
   __syncthreads();
@@ -123,7 +137,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers: 16 elements per thread
-    const f2_t inv2 = f2_pack(p.inv, p.inv);
+    const f2_t inv2 = f2_pack(s_inv, s_inv);
     RingPos rp;
     TileWalker<MAXSEG> walk;
     bool live = true;
@@ -225,26 +239,60 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
         const f2_t pp = COMP ? f2_add(H[u], L[u]) : H[u];
         f2_unpack(f2_mul(pp, inv2), o[2 * u], o[2 * u + 1]);
       }
+      const bool whole = active && e0 >= t.start && e0 + RA_EPT <= t.end;
       if (active) {
-        const bool whole = e0 >= t.start && e0 + RA_EPT <= t.end;
 #pragma unroll
         for (int u = 0; u < RA_EPT; ++u)
           if ((whole || (e0 + u >= t.start && e0 + u < t.end)) && nonfinite(o[u])) ++bad;
-        // Store into the owner's shard at local index, with the widest access the alignment allows.
-        float* dst = p.gbar[t.owner] + (t.loff - t.goff + e0);
-        const int mis = (int)((t.loff - t.goff + e0) & 3);
-        if (whole && mis == 0) {
+      }
+      // Store into the owner's shard at local index.  A thread's 16 values sit at local [Lt, Lt + 16).
+      float* dst = p.gbar[t.owner] + (t.loff - t.goff + e0);
+      const int mis = (int)((t.loff - t.goff + e0) & 3);   // the same for every thread of the tile
+      const bool warp_whole = __all_sync(0xFFFFFFFFu, whole);
+      if (whole && mis == 0) {
+#pragma unroll
+        for (int u = 0; u < RA_EPT; u += 4)
+          *reinterpret_cast<float4*>(dst + u) = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+      } else if (warp_whole) {
+        // Misaligned shard: shift by d = 4 - mis values so every lane stores one 16-byte-aligned chunk
+        // [Lt + d, Lt + d + 16), borrowing d values from the next lane; lane 0 also writes its first d
+        // values, lane 31 (whose next lane is in another warp) writes its own last 16 - d.
+        const int d = 4 - mis;
+        float nb[3];
+#pragma unroll
+        for (int u = 0; u < 3; ++u) nb[u] = __shfl_down_sync(0xFFFFFFFFu, o[u], 1);
+        if (lane == 0) {
+#pragma unroll
+          for (int u = 0; u < 3; ++u)
+            if (u < d) dst[u] = o[u];
+        }
+        if (lane != 31) {
+          float c[RA_EPT];
+#pragma unroll
+          for (int u = 0; u < RA_EPT; ++u) {
+            // c[u] = o[u + d] when that is one of this lane's values, else nb[u + d - 16]
+            float own = o[RA_EPT - 1];
+#pragma unroll
+            for (int q = 1; q <= 3; ++q)
+              if (d == q && u + q < RA_EPT) own = o[u + q];
+            float bor = nb[0];
+#pragma unroll
+            for (int q = 1; q <= 3; ++q)
+              if (d == q && u + q >= RA_EPT) bor = nb[u + q - RA_EPT];
+            c[u] = (u + d < RA_EPT) ? own : bor;
+          }
 #pragma unroll
           for (int u = 0; u < RA_EPT; u += 4)
-            *reinterpret_cast<float4*>(dst + u) = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
-        } else if (whole && mis == 2) {
-#pragma unroll
-          for (int u = 0; u < RA_EPT; u += 2) *reinterpret_cast<float2*>(dst + u) = make_float2(o[u], o[u + 1]);
+            *reinterpret_cast<float4*>(dst + d + u) = make_float4(c[u], c[u + 1], c[u + 2], c[u + 3]);
         } else {
 #pragma unroll
-          for (int u = 0; u < RA_EPT; ++u)
-            if (e0 + u >= t.start && e0 + u < t.end) dst[u] = o[u];
+          for (int u = 1; u < RA_EPT; ++u)
+            if (u >= d) dst[u] = o[u];
         }
+      } else if (active) {
+#pragma unroll
+        for (int u = 0; u < RA_EPT; ++u)
+          if (e0 + u >= t.start && e0 + u < t.end) dst[u] = o[u];
       }
     }
   }
@@ -256,7 +304,8 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
   __syncthreads();
   if (lane == 0 && c) atomicAdd(s_count, c);
   __syncthreads();
-  if (tid == 0) finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2);
+  if (tid == 0)
+    finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2, &p.scaler);
 }
 
 // ============================================================================ update (pass B)
@@ -563,7 +612,8 @@ __global__ void state_init_kernel(dp_step_state_t* st) {
   st->t = 0;
   st->found_inf = 0;
   st->error = 0;
-  st->reserved0 = 0;
+  st->good_steps = 0;
+  st->loss_scale = 0.0f;
   st->nonfinite = 0ull;
   st->b1t = 1.0;
   st->b2t = 1.0;
@@ -571,6 +621,11 @@ __global__ void state_init_kernel(dp_step_state_t* st) {
   st->work_found = 0u;
   st->work_ticket = 0u;
   st->reserved1 = 0ull;
+}
+
+__global__ void scaler_init_kernel(dp_step_state_t* st, float scale) {
+  st->loss_scale = scale;
+  st->good_steps = 0;
 }
 
 // One block waits on a barrier that expects two arrivals but receives one.
@@ -638,6 +693,7 @@ static cudaError_t launch_reduce_t(const Plan& P, const uint16_t* const* g, int 
   prm.n = P.n;
   prm.a = a;
   prm.advance = advance;
+  prm.scaler = s.scaler;
   fill_seg(prm.seg, P);
   auto kern = reduce_kernel<MAXSEG, COMP>;
   // The opt-in shared-memory size is set once per device (not inside a stream capture on later calls).
@@ -803,6 +859,12 @@ cudaError_t launch_allgather(const Plan& P, uint16_t* const* rep, const float* c
 cudaError_t launch_state_init(dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
   ++*launches;
   state_init_kernel<<<1, 1, 0, stream>>>(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scaler_init(dp_step_state_t* st, float scale, cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  scaler_init_kernel<<<1, 1, 0, stream>>>(st, scale);
   return cudaGetLastError();
 }
 
