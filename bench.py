@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=1 << 21, help="elements of the oracle's CPU sample")
     p.add_argument("--psi", type=int, default=0, help="override the parameter count (small profiling cases)")
+    p.add_argument("--path", choices=["two-pass", "single-pass"], default="two-pass",
+                   help="dp_step (reduce + update kernels) or dp_step_single_pass (one pass, two state sets)")
     return p.parse_args()
 
 
@@ -251,9 +253,11 @@ def reference_main(args, wl):
 def config_of(wl, args):
     b1, b2, _, _ = step_bytes(wl)
     return {"workload": wl.description, "psi": wl.psi, "n": wl.n, "a": wl.a, "zero_stage": wl.stage,
-            "layout": wl.layout, "loss_scale": wl.loss_scale, "sum_mode": args.sum, "grad_dtype": "bf16",
+            "layout": wl.layout, "loss_scale": wl.loss_scale, "sum_mode": args.sum, "path": args.path,
+            "grad_dtype": "bf16",
             "state_dtype": "fp32", "bytes_per_param_single_pass": b1, "bytes_per_param_two_pass": b2,
-            "l2": "inputs larger than L2: %.1f GB streamed per step vs 129 MB L2, no flush" % (b2 * wl.psi / 1e9)}
+            "l2": "inputs larger than L2: %.1f GB streamed per step vs 129 MB L2, no flush" % (
+                (b1 if args.path == "single-pass" else b2) * wl.psi / 1e9)}
 
 
 # ----------------------------------------------------------------------------------------------- native leg
@@ -278,7 +282,8 @@ def native_main(args, wl):
     mode = dp.DP_SUM_COMPENSATED if args.sum == "compensated" else dp.DP_SUM_PLAIN
     segs = synth.layout_of(wl)
     layout = dp.Layout(wl.stage, wl.n, wl.psi, segs)
-    bufs = StepBuffers(layout, wl.a, dev)
+    single = args.path == "single-pass"
+    bufs = StepBuffers(layout, wl.a, dev, second_set=single)
     A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
 
     # Inputs: generated on the host into pinned buffers (kept for the end-to-end leg), then copied to HBM.
@@ -291,13 +296,23 @@ def native_main(args, wl):
             host_grads.append(h)
             bufs.grad(r, k).view(torch.int16).copy_(h)
     sd.fill_master(bufs.master, wl, segs, wl.stage)
+    if single:
+        for x, y in zip(bufs.master1, bufs.master):
+            x.copy_(y)
     torch.cuda.synchronize()
     t_gen = time.time() - t_gen
 
     stream = torch.cuda.current_stream()
+
+    def one_step():
+        if single:
+            bufs.step_single_pass(A, wl.loss_scale, mode)
+        else:
+            bufs.reduce(A, wl.loss_scale, mode)
+            bufs.update(A)
+
     for _ in range(args.warmup):
-        bufs.reduce(A, wl.loss_scale, mode)
-        bufs.update(A)
+        one_step()
     torch.cuda.synchronize()
 
     K = args.steps
@@ -314,9 +329,13 @@ def native_main(args, wl):
     clocks.mark(0)
     for k in range(K):
         ev[k][0].record(stream)
-        bufs.reduce(A, wl.loss_scale, mode)
-        ev[k][1].record(stream)
-        bufs.update(A)
+        if single:
+            bufs.step_single_pass(A, wl.loss_scale, mode)
+            ev[k][1].record(stream)
+        else:
+            bufs.reduce(A, wl.loss_scale, mode)
+            ev[k][1].record(stream)
+            bufs.update(A)
     end.record(stream)
     torch.cuda.synchronize()
     clocks.mark(1)
@@ -333,13 +352,15 @@ def native_main(args, wl):
     value = job_throughput(wl.psi, ws, ms)
 
     b1, b2, red_bytes, upd_bytes = step_bytes(wl)
+    if single:
+        red_bytes, upd_bytes = b1, 0     # one kernel streams the single-pass minimum; the repair kernel is idle
     peak, peak_kind = measured_peak()
     red_avg = sum(red_ms) / K
     upd_avg = sum(upd_ms) / K
     red_ach = red_bytes * wl.psi / (red_avg * 1e-3) / 1e9
-    upd_ach = upd_bytes * wl.psi / (upd_avg * 1e-3) / 1e9
-    step_gbs = b2 * wl.psi / (ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name, "reduce")
+    upd_ach = upd_bytes * wl.psi / max(1e-9, upd_avg * 1e-3) / 1e9
+    step_gbs = (b1 if single else b2) * wl.psi / (ms * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name, "single_pass" if single else "reduce")
 
     # End to end through the public call with host buffers: the step's gradients copied from pinned host
     # memory, the step, and the step's status read back, every step.
@@ -355,7 +376,10 @@ def native_main(args, wl):
         for _ in range(KE):
             for q, h in enumerate(host_grads):
                 bufs.grads[q].view(torch.int16).copy_(h, non_blocking=True)
-            bufs.step(A, wl.loss_scale, mode)
+            if single:
+                bufs.step_single_pass(A, wl.loss_scale, mode)
+            else:
+                bufs.step(A, wl.loss_scale, mode)
             host_state.copy_(bufs.state, non_blocking=True)
         s1.record(stream)
         torch.cuda.synchronize()
@@ -390,12 +414,16 @@ def native_main(args, wl):
             "config": config_of(wl, args),
             "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak, "hbm_peak_gbs": peak,
             "hbm_peak_kind": peak_kind,
-            "roofline": {"bound": "hbm", "kernel": "reduce (accumulate + ring reduce-scatter + average + check)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("single-pass reduce + Adam + all-gather" if single else
+                                    "reduce (accumulate + ring reduce-scatter + average + check)"),
                          "achieved": red_ach, "peak": peak, "unit": "GB/s", "frac": red_ach / peak,
                          "traffic": traffic, "bytes_per_launch": red_bytes * wl.psi, "avg_ms": red_avg,
                          "peak_kind": peak_kind},
-            "kernels": {"reduce": {"avg_ms": red_avg, "gbs": red_ach, "bytes_per_param": red_bytes},
-                        "update": {"avg_ms": upd_avg, "gbs": upd_ach, "bytes_per_param": upd_bytes}},
+            "kernels": ({"single_pass": {"avg_ms": red_avg, "gbs": red_ach, "bytes_per_param": red_bytes},
+                         "repair": {"avg_ms": upd_avg}} if single else
+                        {"reduce": {"avg_ms": red_avg, "gbs": red_ach, "bytes_per_param": red_bytes},
+                         "update": {"avg_ms": upd_avg, "gbs": upd_ach, "bytes_per_param": upd_bytes}}),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "status": {"skipped_last_step": skipped, "error": err}, "setup_s": t_gen,
         }

@@ -129,7 +129,7 @@ typedef struct {
   uint32_t work_found;  /* kernel-internal, zero between calls */
   uint32_t work_ticket; /* kernel-internal, zero between calls */
   float loss_scale;   /* dynamic loss scale used by dp_step_scaled (set by dp_scaler_init) */
-  uint32_t reserved1;
+  uint32_t cur_set;   /* dp_step_single_pass: which of the two master/m/v sets is current (0 or 1) */
 } dp_step_state_t;
 
 /* Dynamic loss-scale policy of dp_step_scaled.  After each reduction:
@@ -294,6 +294,24 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
                            const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
                            const dp_scaler_t* scaler, int32_t sum_mode, float* const* gbar_shard, void* ws,
                            dp_step_state_t* d_state, dp_stream_t stream);
+
+/* The fused step in ONE pass over memory (one reduce-and-update kernel, plus a
+ * repair kernel that does work only on a skipped step).  The optimizer state
+ * is double-buffered: master, m and v are host arrays of 2n device pointers,
+ * set 0 (entries 0..n-1) and set 1 (entries n..2n-1), each like dp_step's.
+ * d_state->cur_set (0 after dp_state_init) names the current set; the kernel
+ * reads it and writes the other set, and the reduction's last CTA makes the
+ * other set current only if no value was non-finite.  gbar never reaches
+ * memory, so the step streams the single-pass minimum 2na + 24 + 2n bytes per
+ * parameter instead of dp_step's 2na + 32 + 2n.  Replicas are written in
+ * place while the skip decision is still open; on a skipped step the repair
+ * kernel rewrites them as bf16_rne of the (unchanged) current master, so a
+ * skipped step leaves the replicas as they were provided they held
+ * bf16_rne(master) before it -- the invariant every applied step
+ * establishes.  Results are bit-identical to dp_step.  Stages 1-3 only. */
+dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                                const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                                float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream);
 
 /* Reads found_inf and error of *d_state into host ints after synchronising
  * the stream (the one blocking call).  skipped / err may be NULL. */

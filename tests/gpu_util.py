@@ -56,8 +56,8 @@ def make_case(wl: synth.Workload, stage: Optional[int] = None, segs=None, t: int
     return Case(wl, segs, stage, dp.Layout(stage, wl.n, wl.psi, segs), grads, master, m, v, t)
 
 
-def upload(c: Case, device="cuda") -> StepBuffers:
-    b = StepBuffers(c.layout, c.wl.a, device)
+def upload(c: Case, device="cuda", second_set: bool = False) -> StepBuffers:
+    b = StepBuffers(c.layout, c.wl.a, device, second_set=second_set)
     for q, g in enumerate(c.grads):
         b.grads[q].copy_(sd.bf16_from_bits(g))
     sd.place_full(b.master, c.master, c.segs, c.stage)

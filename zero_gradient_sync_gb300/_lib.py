@@ -39,7 +39,7 @@ class dp_step_state_t(ctypes.Structure):
     _fields_ = [("t", c_i32), ("found_inf", c_i32), ("error", c_i32), ("good_steps", c_i32), ("nonfinite", c_u64),
                 ("b1t", ctypes.c_double), ("b2t", ctypes.c_double), ("work_count", c_u64),
                 ("work_found", ctypes.c_uint32), ("work_ticket", ctypes.c_uint32), ("loss_scale", c_f32),
-                ("reserved1", ctypes.c_uint32)]
+                ("cur_set", ctypes.c_uint32)]
 
 
 class dp_scaler_t(ctypes.Structure):
@@ -86,6 +86,8 @@ def _load() -> ctypes.CDLL:
         "dp_scaler_init": (c_i32, [c_vp, c_f32, c_vp]),
         "dp_step_scaled": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, P(dp_scaler_t), c_i32,
                                    c_vp, c_vp, c_vp, c_vp]),
+        "dp_step_single_pass": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32,
+                                        c_vp, c_vp]),
         "dp_step_static": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32,
                                    c_vp, c_vp]),
     }
@@ -274,6 +276,22 @@ def dp_step_update(replicas, master, m, v, gbar_shard, ws, layout: Layout, adam_
                               ctypes.byref(layout.c), adam_, _ptr(state), _stream(stream)), "dp_step_update")
 
 
+def dp_step_single_pass(replicas, master2, m2, v2, grads, a: int, layout: Layout, adam_: dp_adam_t,
+                        loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED, state=None, stream=None) -> None:
+    """One-pass step with double-buffered optimizer state: master2, m2, v2 are lists of 2n tensors (set 0, then
+    set 1); the state's cur_set names the current set."""
+    lens = layout.shard_lens() * 2
+    for name, ts in (("master", master2), ("m", m2), ("v", v2)):
+        if len(ts) != 2 * layout.n:
+            raise ValueError("%s: need 2n = %d tensors" % (name, 2 * layout.n))
+        _check_tensors(ts, 4, lens, name)
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    _check_tensors(grads, 2, [layout.psi] * len(grads), "grads")
+    _check(LIB.dp_step_single_pass(_ptr_array(replicas), _ptr_array(master2), _ptr_array(m2), _ptr_array(v2),
+                                   _ptr_array(grads), a, ctypes.byref(layout.c), adam_, loss_scale, sum_mode,
+                                   _ptr(state), _stream(stream)), "dp_step_single_pass")
+
+
 STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -365,4 +383,4 @@ def read_state(state) -> dict:
     s = dp_step_state_t.from_buffer_copy(raw)
     return {"t": s.t, "found_inf": s.found_inf, "error": s.error, "nonfinite": s.nonfinite, "b1t": s.b1t,
             "b2t": s.b2t, "work_count": s.work_count, "work_found": s.work_found, "work_ticket": s.work_ticket,
-            "good_steps": s.good_steps, "loss_scale": s.loss_scale}
+            "good_steps": s.good_steps, "loss_scale": s.loss_scale, "cur_set": s.cur_set}

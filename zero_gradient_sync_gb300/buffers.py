@@ -16,7 +16,7 @@ from ._lib import DP_SUM_COMPENSATED, Layout
 
 
 class StepBuffers:
-    def __init__(self, layout: Layout, a: int, device=None, with_grads: bool = True):
+    def __init__(self, layout: Layout, a: int, device=None, with_grads: bool = True, second_set: bool = False):
         self.layout = layout
         self.n, self.a, self.psi = layout.n, int(a), layout.psi
         self.device = torch.device(device or "cuda")
@@ -32,6 +32,21 @@ class StepBuffers:
         self.v = [torch.zeros(L, dtype=torch.float32, device=dev) for L in lens]
         self.gbar = [torch.empty(L, dtype=torch.float32, device=dev) for L in shard]
         self.state = _lib.new_state(dev)
+        # Single pass: a second master/m/v set; set 0 is master/m/v above.
+        self.master1 = [torch.empty(L, dtype=torch.float32, device=dev) for L in lens] if second_set else []
+        self.m1 = [torch.zeros(L, dtype=torch.float32, device=dev) for L in lens] if second_set else []
+        self.v1 = [torch.zeros(L, dtype=torch.float32, device=dev) for L in lens] if second_set else []
+
+    def step_single_pass(self, adam_: _lib.dp_adam_t, loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED,
+                         stream=None) -> None:
+        _lib.dp_step_single_pass(self.replicas, self.master + self.master1, self.m + self.m1, self.v + self.v1,
+                                 self.grads, self.a, self.layout, adam_, loss_scale, sum_mode, state=self.state,
+                                 stream=stream)
+
+    def current(self):
+        """The current (master, m, v) set of a single-pass run."""
+        cur = _lib.read_state(self.state)["cur_set"]
+        return (self.master, self.m, self.v) if cur == 0 else (self.master1, self.m1, self.v1)
 
     def grad(self, r: int, k: int) -> torch.Tensor:
         return self.grads[r * self.a + k]

@@ -501,6 +501,31 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
 }
 
+dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                                const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                                float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  if (P.stage == 0) return fail(DP_ERR_INVALID_ARG, "dp_step_single_pass: stage 0 (full replicas) is not supported");
+  if (a < 1 || (int64_t)a * P.n > DP_MAX_NA)
+    return fail(DP_ERR_INVALID_ARG, "a = %d: need 1 <= a and n * a <= %d", a, DP_MAX_NA);
+  StepScalars s;
+  if ((st = scalars(P, &adam, loss_scale, sum_mode, s)) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)grads, P.n * a, "grads")) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  int64_t lens2[2 * DP_MAX_N];
+  for (int r = 0; r < P.n; ++r) lens2[r] = lens2[P.n + r] = P.shard_len[r];
+  if ((st = check_ptr_array((const void* const*)master, 2 * P.n, "master (2 sets)", lens2)) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)m, 2 * P.n, "m (2 sets)", lens2)) != DP_OK) return st;
+  if ((st = check_ptr_array((const void* const*)v, 2 * P.n, "v (2 sets)", lens2)) != DP_OK) return st;
+  if ((st = check_state(d_state)) != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_single_pass(P, grads, a, replicas, master, m, v, s, d_state, (cudaStream_t)stream,
+                                         &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "single-pass launch");
+}
+
 dp_status_t dp_read_status(const dp_step_state_t* d_state, int32_t* skipped, int32_t* err, dp_stream_t stream) {
   dp_status_t st = check_state(d_state);
   if (st != DP_OK) return st;

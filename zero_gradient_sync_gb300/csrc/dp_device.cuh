@@ -268,7 +268,7 @@ struct ScalerK {
 
 __device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned long long cta_count, int cta_found,
                                                  int advance, double b1, double b2,
-                                                 const ScalerK* scaler = nullptr) {
+                                                 const ScalerK* scaler = nullptr, int flip_set = 0) {
   if (cta_count) atomicAdd(reinterpret_cast<unsigned long long*>(&st->work_count), cta_count);
   if (cta_found) atomicOr(&st->work_found, 1u);
   __threadfence();
@@ -285,6 +285,7 @@ __device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned l
       st->t += 1;
       st->b1t *= b1;
       st->b2t *= b2;
+      if (flip_set) st->cur_set ^= 1u;
     }
     if (scaler && scaler->enabled && err == 0) {
       float sc = st->loss_scale;

@@ -36,6 +36,9 @@ dp_status_t report_error(dp_status_t s, const char* msg);
 // Each launcher returns the launch's cudaError_t and adds to *launches.
 cudaError_t launch_reduce(const Plan& P, const uint16_t* const* g, int a, float* const* gbar, const StepScalars& s,
                           int advance, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_single_pass(const Plan& P, const uint16_t* const* g, int a, uint16_t* const* rep,
+                               float* const* master2, float* const* m2, float* const* v2, const StepScalars& s,
+                               dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
 cudaError_t launch_update(const Plan& P, uint16_t* const* rep, float* const* master, float* const* m,
                           float* const* v, const float* const* gbar, const StepScalars& s,
                           const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);

@@ -29,7 +29,13 @@ constexpr int RA_EPT = 16;                     // elements per consumer thread: 
 constexpr int RA_THREADS = RA_CTHREADS + 32;   // + one producer warp: 16 warps, 4 per SM sub-partition
 constexpr int RA_STAGES = 12;
 constexpr int RA_STAGE_BYTES = TILE * 2;       // one tile of one bf16 input: a 15 KB bulk copy
-constexpr int RA_SMEM = RA_STAGES * RA_STAGE_BYTES + 2 * RA_STAGES * 8 + 32;
+constexpr int RA_GBAR_FLOATS = TILE + 16;      // single pass: the tile's gbar (+16: last group's overhang)
+constexpr int RA_EXTRA_FUSED = RA_GBAR_FLOATS * 4 + TILE * 2;   // + the tile's bf16 staging
+template <bool FUSED>
+__host__ __device__ constexpr int ra_bar_offset() { return RA_STAGES * RA_STAGE_BYTES + (FUSED ? RA_EXTRA_FUSED : 0); }
+template <bool FUSED>
+__host__ __device__ constexpr int ra_smem() { return ra_bar_offset<FUSED>() + 2 * RA_STAGES * 8 + 32; }
+static_assert(ra_smem<true>() + 64 <= 227 * 1024, "single-pass shared memory fits one CTA");
 static_assert(TILE == RA_CTHREADS * RA_EPT, "one 16-element group per consumer thread");
 static_assert(RA_STAGE_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
 
@@ -43,6 +49,12 @@ struct ReduceParams {
   float inv;
   int32_t n, a, advance;
   ScalerK scaler;    // enabled: unscale by the device-resident scale, then update it
+  // single pass only: the two optimizer-state sets, the replicas, Adam constants
+  float* st_master[2][DP_MAX_N];
+  float* st_m[2][DP_MAX_N];
+  float* st_v[2][DP_MAX_N];
+  uint16_t* rep[DP_MAX_N];
+  float lr, b1f, b2f, eps, omb1, omb2;
   SegTable<MAXSEG> seg;
 };
 
@@ -58,15 +70,101 @@ struct RingPos {
   }
 };
 
-template <int MAXSEG, bool COMP>
+// Four bf16 values into a staging tile at element offset `off` (any alignment).
+__device__ __forceinline__ void stage_bf16x4(uint16_t* sb, int64_t off, uint32_t w0, uint32_t w1) {
+  if ((off & 3) == 0) {
+    *reinterpret_cast<uint2*>(sb + off) = make_uint2(w0, w1);
+  } else if ((off & 1) == 0) {
+    *reinterpret_cast<uint32_t*>(sb + off) = w0;
+    *reinterpret_cast<uint32_t*>(sb + off + 2) = w1;
+  } else {
+    sb[off] = (uint16_t)(w0 & 0xFFFFu);
+    sb[off + 1] = (uint16_t)(w0 >> 16);
+    sb[off + 2] = (uint16_t)(w1 & 0xFFFFu);
+    sb[off + 3] = (uint16_t)(w1 >> 16);
+  }
+}
+
+// Single pass: Adam on the tile's local 4-groups with gbar from shared memory (indexed by global position),
+// old state from set `cur`, new state into the other set, bf16 of the new master into the staging tile.
+template <int MAXSEG>
+__device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, const Tile& t, const AdamK& K, int cur,
+                                             const float* s_g, uint16_t* s_stage, int tid) {
+  constexpr int UG = 2;
+  const int64_t delta = t.loff - t.goff;
+  const int64_t cb = (t.start / TILE) * TILE;
+  const int64_t js = t.start + delta, je = t.end + delta;
+  const int64_t jlo = (js + 3) & ~int64_t(3), jhi = je & ~int64_t(3);
+  const int ngr = jhi > jlo ? (int)((jhi - jlo) >> 2) : 0;
+  const float* M = p.st_master[cur][t.owner];
+  const float* Mm = p.st_m[cur][t.owner];
+  const float* Vv = p.st_v[cur][t.owner];
+  float* M2 = p.st_master[cur ^ 1][t.owner];
+  float* Mm2 = p.st_m[cur ^ 1][t.owner];
+  float* Vv2 = p.st_v[cur ^ 1][t.owner];
+  const bool galign = ((delta & 3) == 0);
+  for (int base = 0; base < ngr; base += UG * RA_CTHREADS) {
+    float4 t4[UG], m4[UG], v4[UG], g4[UG];
+#pragma unroll
+    for (int u = 0; u < UG; ++u) {
+      const int gq = base + tid + u * RA_CTHREADS;
+      if (gq < ngr) {
+        const int64_t jj = jlo + 4 * (int64_t)gq;
+        t4[u] = *reinterpret_cast<const float4*>(M + jj);
+        m4[u] = *reinterpret_cast<const float4*>(Mm + jj);
+        v4[u] = *reinterpret_cast<const float4*>(Vv + jj);
+        const float* gs = s_g + (jj - delta - cb);
+        g4[u] = galign ? *reinterpret_cast<const float4*>(gs) : make_float4(gs[0], gs[1], gs[2], gs[3]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UG; ++u) {
+      const int gq = base + tid + u * RA_CTHREADS;
+      if (gq < ngr) {
+        const int64_t jj = jlo + 4 * (int64_t)gq;
+        adam1(g4[u].x, t4[u].x, m4[u].x, v4[u].x, K);
+        adam1(g4[u].y, t4[u].y, m4[u].y, v4[u].y, K);
+        adam1(g4[u].z, t4[u].z, m4[u].z, v4[u].z, K);
+        adam1(g4[u].w, t4[u].w, m4[u].w, v4[u].w, K);
+        *reinterpret_cast<float4*>(M2 + jj) = t4[u];
+        *reinterpret_cast<float4*>(Mm2 + jj) = m4[u];
+        *reinterpret_cast<float4*>(Vv2 + jj) = v4[u];
+        stage_bf16x4(s_stage, jj - delta - cb, bf16x2_rn(t4[u].x, t4[u].y), bf16x2_rn(t4[u].z, t4[u].w));
+      }
+    }
+  }
+  // Ragged ends of the tile in local space (at most 3 elements each).
+  int64_t jx = -1;
+  if (tid < 4) {
+    jx = js + tid;
+    if (jx >= (jlo < je ? jlo : je)) jx = -1;
+  } else if (tid < 8) {
+    jx = (jhi > jlo ? jhi : jlo) + (tid - 4);
+    if (jx >= je) jx = -1;
+  }
+  if (jx >= 0) {
+    float th = M[jx], mm = Mm[jx], vv = Vv[jx];
+    adam1(s_g[jx - delta - cb], th, mm, vv, K);
+    M2[jx] = th;
+    Mm2[jx] = mm;
+    Vv2[jx] = vv;
+    s_stage[jx - delta - cb] = bf16_rn(th);
+  }
+}
+
+template <int MAXSEG, bool COMP, bool FUSED>
 __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceParams<MAXSEG> p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RA_STAGES * RA_STAGE_BYTES);
+  float* s_g = reinterpret_cast<float*>(smem + RA_STAGES * RA_STAGE_BYTES);
+  uint16_t* s_stage = reinterpret_cast<uint16_t*>(smem + RA_STAGES * RA_STAGE_BYTES + RA_GBAR_FLOATS * 4);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ra_bar_offset<FUSED>());
   uint64_t* empty = full + RA_STAGES;
   volatile int* s_abort = reinterpret_cast<volatile int*>(empty + RA_STAGES);
   unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + RA_STAGES + 1);
   __shared__ float s_inv;
+  __shared__ float s_k[2];
+  __shared__ int s_cur;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = p.n, a = p.a;
@@ -93,6 +191,13 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
       }
     }
     s_inv = inv;
+    if (FUSED) {
+      // Bias corrections of the step being taken (t + 1): the same double products the finish stores.
+      const volatile dp_step_state_t* vs = p.state;
+      s_k[0] = (float)((double)p.lr / (1.0 - vs->b1t * p.beta1));
+      s_k[1] = (float)(1.0 / sqrt(1.0 - vs->b2t * p.beta2));
+      s_cur = (int)(vs->cur_set & 1u);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -245,6 +350,50 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
         for (int u = 0; u < RA_EPT; ++u)
           if ((whole || (e0 + u >= t.start && e0 + u < t.end)) && nonfinite(o[u])) ++bad;
       }
+      if constexpr (FUSED) {
+        // Single pass: hand the tile's gbar to its update through shared memory (indexed by global position).
+        const int64_t cb = (t.start / TILE) * TILE;
+        named_bar_sync(1, RA_CTHREADS);    // the previous tile's update is done with s_g and s_stage
+        if (tid == 0) bulk_wait_read<0>(); // and its replica stores have read s_stage
+        if (active) {
+          float4* gp = reinterpret_cast<float4*>(s_g + (e0 - cb));
+#pragma unroll
+          for (int u = 0; u < RA_EPT; u += 4) gp[u / 4] = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+        }
+        named_bar_sync(1, RA_CTHREADS);
+        AdamK K;
+        K.b1 = p.b1f; K.b2 = p.b2f; K.omb1 = p.omb1; K.omb2 = p.omb2; K.eps = p.eps;
+        K.step = s_k[0];
+        K.rsbc2 = s_k[1];
+        fused_update(p, t, K, s_cur, s_g, s_stage, tid);
+        fence_proxy_async_smem();
+        named_bar_sync(1, RA_CTHREADS);
+        // All-gather: the staged bf16 tile into every replica (16-byte-aligned interior by bulk copies).
+        const int64_t ilo = (t.start + 7) & ~int64_t(7), ihi = t.end & ~int64_t(7);
+        if (tid == 0) {
+          if (ihi > ilo) {
+            const uint32_t src = smem_u32(s_stage + (ilo - cb));
+            const uint32_t bytes = (uint32_t)(ihi - ilo) * 2u;
+            for (int rr = 0; rr < n; ++rr) bulk_s2g(p.rep[rr] + ilo, src, bytes);
+          }
+          bulk_commit();
+        }
+        if (tid < 16) {
+          int64_t ix = -1;
+          if (tid < 8) {
+            ix = t.start + tid;
+            if (ix >= (ilo < t.end ? ilo : t.end)) ix = -1;
+          } else {
+            ix = (ihi > ilo ? ihi : ilo) + (tid - 8);
+            if (ix >= t.end) ix = -1;
+          }
+          if (ix >= 0) {
+            const uint16_t b = s_stage[ix - cb];
+            for (int rr = 0; rr < n; ++rr) p.rep[rr][ix] = b;
+          }
+        }
+        continue;
+      }
       // Store into the owner's shard at local index.  A thread's 16 values sit at local [Lt, Lt + 16).
       float* dst = p.gbar[t.owner] + (t.loff - t.goff + e0);
       const int mis = (int)((t.loff - t.goff + e0) & 3);   // the same for every thread of the tile
@@ -304,8 +453,10 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
   __syncthreads();
   if (lane == 0 && c) atomicAdd(s_count, c);
   __syncthreads();
+  if (FUSED && tid == 0) bulk_wait_all();   // the last tile's replica stores
   if (tid == 0)
-    finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2, &p.scaler);
+    finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2, &p.scaler,
+                     FUSED ? 1 : 0);
 }
 
 // ============================================================================ update (pass B)
@@ -341,19 +492,6 @@ __device__ __forceinline__ bool update_prologue(const dp_step_state_t* st, float
   return true;
 }
 
-__device__ __forceinline__ void stage_bf16x4(uint16_t* sb, int64_t off, uint32_t w0, uint32_t w1) {
-  if ((off & 3) == 0) {
-    *reinterpret_cast<uint2*>(sb + off) = make_uint2(w0, w1);
-  } else if ((off & 1) == 0) {
-    *reinterpret_cast<uint32_t*>(sb + off) = w0;
-    *reinterpret_cast<uint32_t*>(sb + off + 2) = w1;
-  } else {
-    sb[off] = (uint16_t)(w0 & 0xFFFFu);
-    sb[off + 1] = (uint16_t)(w0 >> 16);
-    sb[off + 2] = (uint16_t)(w1 & 0xFFFFu);
-    sb[off + 3] = (uint16_t)(w1 >> 16);
-  }
-}
 
 // Stages 1-3: shard arrays in local index space.  REPL: also all-gather.
 template <int MAXSEG, bool REPL>
@@ -614,13 +752,13 @@ __global__ void state_init_kernel(dp_step_state_t* st) {
   st->error = 0;
   st->good_steps = 0;
   st->loss_scale = 0.0f;
+  st->cur_set = 0u;
   st->nonfinite = 0ull;
   st->b1t = 1.0;
   st->b2t = 1.0;
   st->work_count = 0ull;
   st->work_found = 0u;
   st->work_ticket = 0u;
-  st->reserved1 = 0ull;
 }
 
 __global__ void scaler_init_kernel(dp_step_state_t* st, float scale) {
@@ -679,12 +817,21 @@ static int occupancy_grid(K kernel, int threads, size_t smem, int ntiles) {
   return (int)(g < 1 ? 1 : g);
 }
 
-template <int MAXSEG, bool COMP>
+// Single-pass inputs beyond the reduction's: optimizer-state sets and replicas.
+struct FusedArgs {
+  float* const* master;  // 2n pointers: set 0 then set 1
+  float* const* m;
+  float* const* v;
+  uint16_t* const* rep;  // n
+};
+
+template <int MAXSEG, bool COMP, bool FUSED>
 static cudaError_t launch_reduce_t(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
-                                   const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream) {
+                                   const StepScalars& s, int advance, dp_step_state_t* st, const FusedArgs* fa,
+                                   cudaStream_t stream) {
   ReduceParams<MAXSEG> prm;
   for (int q = 0; q < P.n * a; ++q) prm.g[q] = g[q];
-  for (int r = 0; r < P.n; ++r) prm.gbar[r] = gbar[r];
+  for (int r = 0; r < P.n; ++r) prm.gbar[r] = gbar ? gbar[r] : nullptr;
   prm.state = st;
   prm.timeout_ns = s.timeout_ns;
   prm.beta1 = (double)s.beta1;
@@ -694,22 +841,39 @@ static cudaError_t launch_reduce_t(const Plan& P, const uint16_t* const* g, int 
   prm.a = a;
   prm.advance = advance;
   prm.scaler = s.scaler;
+  if (fa) {
+    for (int r = 0; r < P.n; ++r) {
+      for (int k = 0; k < 2; ++k) {
+        prm.st_master[k][r] = fa->master[k * P.n + r];
+        prm.st_m[k][r] = fa->m[k * P.n + r];
+        prm.st_v[k][r] = fa->v[k * P.n + r];
+      }
+      prm.rep[r] = fa->rep[r];
+    }
+  }
+  prm.lr = s.lr;
+  prm.b1f = s.beta1;
+  prm.b2f = s.beta2;
+  prm.eps = s.eps;
+  prm.omb1 = s.omb1;
+  prm.omb2 = s.omb2;
   fill_seg(prm.seg, P);
-  auto kern = reduce_kernel<MAXSEG, COMP>;
+  auto kern = reduce_kernel<MAXSEG, COMP, FUSED>;
+  constexpr int smem = ra_smem<FUSED>();
   // The opt-in shared-memory size is set once per device (not inside a stream capture on later calls).
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RA_SMEM);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   // Every CTA takes part in the grid-wide finish, so at least one CTA runs even with no tiles.
   int grid = sm_count();
   if (P.ntiles < grid) grid = P.ntiles > 0 ? P.ntiles : 1;
-  kern<<<grid, RA_THREADS, RA_SMEM, stream>>>(prm);
+  kern<<<grid, RA_THREADS, smem, stream>>>(prm);
   return cudaGetLastError();
 }
 
@@ -718,10 +882,65 @@ cudaError_t launch_reduce(const Plan& P, const uint16_t* const* g, int a, float*
   ++*launches;
   const bool comp = s.mode == DP_SUM_COMPENSATED;
   if (P.nseg <= SMALL_SEG)
-    return comp ? launch_reduce_t<SMALL_SEG, true>(P, g, a, gbar, s, advance, st, stream)
-                : launch_reduce_t<SMALL_SEG, false>(P, g, a, gbar, s, advance, st, stream);
-  return comp ? launch_reduce_t<BIG_SEG, true>(P, g, a, gbar, s, advance, st, stream)
-              : launch_reduce_t<BIG_SEG, false>(P, g, a, gbar, s, advance, st, stream);
+    return comp ? launch_reduce_t<SMALL_SEG, true, false>(P, g, a, gbar, s, advance, st, nullptr, stream)
+                : launch_reduce_t<SMALL_SEG, false, false>(P, g, a, gbar, s, advance, st, nullptr, stream);
+  return comp ? launch_reduce_t<BIG_SEG, true, false>(P, g, a, gbar, s, advance, st, nullptr, stream)
+              : launch_reduce_t<BIG_SEG, false, false>(P, g, a, gbar, s, advance, st, nullptr, stream);
+}
+
+// After a single-pass step: if it was skipped, rewrite the replicas as bf16 of the current (unchanged) master.
+template <int MAXSEG>
+struct RepairParams {
+  uint16_t* rep[DP_MAX_N];
+  const float* master[2][DP_MAX_N];
+  const dp_step_state_t* state;
+  int32_t n;
+  SegTable<MAXSEG> seg;
+};
+
+template <int MAXSEG>
+__global__ void __launch_bounds__(256) repair_kernel(const __grid_constant__ RepairParams<MAXSEG> p) {
+  const volatile dp_step_state_t* vs = p.state;
+  if (!vs->found_inf) return;
+  const int cur = (int)(vs->cur_set & 1u);
+  for (int tile = blockIdx.x; tile < p.seg.ntiles; tile += gridDim.x) {
+    const Tile t = tile_at(p.seg, tile);
+    const float* M = p.master[cur][t.owner];
+    for (int64_t e = t.start + threadIdx.x; e < t.end; e += blockDim.x) {
+      const uint16_t b = bf16_rn(M[t.loff + (e - t.goff)]);
+      for (int r = 0; r < p.n; ++r) p.rep[r][e] = b;
+    }
+  }
+}
+
+template <int MAXSEG>
+static cudaError_t launch_single_t(const Plan& P, const uint16_t* const* g, int a, const StepScalars& s,
+                                   dp_step_state_t* st, const FusedArgs& fa, cudaStream_t stream) {
+  cudaError_t e = s.mode == DP_SUM_COMPENSATED
+                      ? launch_reduce_t<MAXSEG, true, true>(P, g, a, nullptr, s, 1, st, &fa, stream)
+                      : launch_reduce_t<MAXSEG, false, true>(P, g, a, nullptr, s, 1, st, &fa, stream);
+  if (e != cudaSuccess) return e;
+  RepairParams<MAXSEG> rp;
+  for (int r = 0; r < P.n; ++r) {
+    rp.rep[r] = fa.rep[r];
+    rp.master[0][r] = fa.master[r];
+    rp.master[1][r] = fa.master[P.n + r];
+  }
+  rp.state = st;
+  rp.n = P.n;
+  fill_seg(rp.seg, P);
+  auto k = repair_kernel<MAXSEG>;
+  k<<<occupancy_grid(k, 256, 0, P.ntiles > 0 ? P.ntiles : 1), 256, 0, stream>>>(rp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_single_pass(const Plan& P, const uint16_t* const* g, int a, uint16_t* const* rep,
+                               float* const* master2, float* const* m2, float* const* v2, const StepScalars& s,
+                               dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  *launches += 2;
+  const FusedArgs fa{master2, m2, v2, rep};
+  if (P.nseg <= SMALL_SEG) return launch_single_t<SMALL_SEG>(P, g, a, s, st, fa, stream);
+  return launch_single_t<BIG_SEG>(P, g, a, s, st, fa, stream);
 }
 
 template <int MAXSEG>
