@@ -44,6 +44,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=1 << 21, help="elements of the oracle's CPU sample")
     p.add_argument("--psi", type=int, default=0, help="override the parameter count (small profiling cases)")
+    p.add_argument("--checkpoint", default="",
+                   help="time sharded checkpoint save / reshard-load of the workload's optimizer state under this "
+                        "directory instead of the step (prints its own JSON line)")
     p.add_argument("--path", choices=["two-pass", "single-pass"], default="two-pass",
                    help="dp_step (reduce + update kernels) or dp_step_single_pass (one pass, two state sets)")
     return p.parse_args()
@@ -434,6 +437,135 @@ def native_main(args, wl):
     return 0
 
 
+def checkpoint_main(args, wl):
+    """Sharded checkpoint of the workload's fp32 master/m/v (12 bytes a parameter): --steps saves, each
+    followed by a load into a layout of n/2 ranks (a reshard), wall-clock timed (the calls are host-synchronous).
+    Bounds measured on the same box: the pinned device-to-host / host-to-device copy rate and the file system's
+    multi-threaded write / read rate for the same bytes."""
+    import shutil
+    from concurrent.futures import ThreadPoolExecutor
+
+    import torch
+
+    import synth
+    import zero_gradient_sync_gb300 as dp
+
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    lay = dp.Layout(wl.stage, wl.n, wl.psi, synth.layout_of(wl))
+    n2 = max(1, wl.n // 2)
+    lay2 = dp.Layout.even(wl.psi, n2, stage=max(1, wl.stage))
+    g = torch.Generator(device=dev).manual_seed(11)
+    src = [[torch.randn(L, device=dev, generator=g) for L in lay.state_lens()] for _ in range(3)]
+    dst = [[torch.empty(L, device=dev) for L in lay2.state_lens()] for _ in range(3)]
+    state = dp.new_state(dev)
+    nbytes = 12 * wl.psi
+    root = os.path.abspath(args.checkpoint)
+    os.makedirs(root, exist_ok=True)
+
+    def fresh(tag):
+        d = os.path.join(root, tag)
+        if os.path.isdir(d):
+            shutil.rmtree(d)
+
+    saves, loads = [], []
+    for k in range(args.warmup + args.steps):
+        tag = "bench%d" % (k % 2)
+        fresh(tag)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dp.dp_checkpoint_save(root, tag, lay, *src, state)
+        t1 = time.perf_counter()
+        dp.dp_checkpoint_load(root, tag, lay2, *dst, state, verify=False)
+        t2 = time.perf_counter()
+        if k >= args.warmup:
+            saves.append(t1 - t0)
+            loads.append(t2 - t1)
+    t0 = time.perf_counter()
+    dp.dp_checkpoint_load(root, None, lay2, *dst, state, verify=True)
+    t_verify = time.perf_counter() - t0
+    ok = all(torch.equal(torch.cat(a).view(torch.int32), torch.cat(b).view(torch.int32)) for a, b in zip(src, dst))
+
+    # bounds: pinned host<->device copies, and plain multi-threaded file writes / reads of the same bytes
+    chunk = 1 << 24
+    pin = torch.empty(nbytes // 4, dtype=torch.float32, pin_memory=True)
+    flat = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    pin.copy_(flat, non_blocking=True)
+    torch.cuda.synchronize()
+    d2h = nbytes / (time.perf_counter() - t0) / 1e9
+    t0 = time.perf_counter()
+    flat.copy_(pin, non_blocking=True)
+    torch.cuda.synchronize()
+    h2d = nbytes / (time.perf_counter() - t0) / 1e9
+    view = memoryview(pin.numpy()).cast("B")
+    workers = min(8, os.cpu_count() or 1)
+    part = -(-nbytes // workers)
+    rawdir = os.path.join(root, "raw")
+    os.makedirs(rawdir, exist_ok=True)
+
+    def write_part(i):
+        path = os.path.join(rawdir, "p%d" % i)
+        fd = os.open(path, os.O_WRONLY | os.O_CREAT | os.O_TRUNC, 0o644)
+        try:
+            lo, hi = i * part, min(nbytes, (i + 1) * part)
+            for o in range(lo, hi, chunk):
+                os.write(fd, view[o:min(hi, o + chunk)])
+            os.fsync(fd)
+        finally:
+            os.close(fd)
+
+    def read_part(i):
+        path = os.path.join(rawdir, "p%d" % i)
+        with open(path, "rb", buffering=0) as f:
+            while f.read(chunk):
+                pass
+
+    with ThreadPoolExecutor(workers) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(write_part, range(workers)))
+        fs_w = nbytes / (time.perf_counter() - t0) / 1e9
+        t0 = time.perf_counter()
+        list(ex.map(read_part, range(workers)))
+        fs_r = nbytes / (time.perf_counter() - t0) / 1e9
+    shutil.rmtree(rawdir)
+    for tag in ("bench0", "bench1"):
+        fresh(tag)
+
+    save_s, load_s = statistics.median(saves), statistics.median(loads)
+    out = {
+        "metric": "sharded checkpoint of fp32 master/m/v: save and reshard-load GB/s",
+        "value": round(nbytes / save_s / 1e9, 3), "unit": "GB/s (save)", "higher_is_better": True,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * save_s, 2),
+        "load_gbs": round(nbytes / load_s / 1e9, 3), "load_verified_gbs": round(nbytes / t_verify / 1e9, 3),
+        "bytes": nbytes, "bit_exact": ok,
+        "bounds": {"d2h_gbs": round(d2h, 2), "h2d_gbs": round(h2d, 2), "fs_write_fsync_gbs": round(fs_w, 3),
+                   "fs_read_gbs": round(fs_r, 3), "threads": workers},
+        "config": {"workload": wl.name, "psi": wl.psi, "n": wl.n, "stage": wl.stage, "layout": wl.layout,
+                   "reshard_to_n": n2, "dir_fs": _fs_type(root)},
+        "data": "synthetic", "dtype": "f32",
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def _fs_type(path: str) -> str:
+    try:
+        best, kind = "", "unknown"
+        with open("/proc/mounts") as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) > 2 and path.startswith(parts[1]) and len(parts[1]) > len(best):
+                    best, kind = parts[1], parts[2]
+        return kind
+    except OSError:
+        return "unknown"
+
+
 def main():
     args = parse()
     import synth
@@ -444,6 +576,8 @@ def main():
         wl = wl.with_(psi=args.psi, description=wl.description + " [psi overridden to %d]" % args.psi)
     if args.impl == "reference":
         return reference_main(args, wl)
+    if args.checkpoint:
+        return checkpoint_main(args, wl)
     return native_main(args, wl)
 
 

@@ -68,7 +68,8 @@ typedef enum {
   DP_ERR_INVALID_ARG = 1, /* bad size, layout, pointer or scalar; nothing launched */
   DP_ERR_ALIGNMENT = 2,   /* a device base pointer is not 16-byte aligned; nothing launched */
   DP_ERR_CUDA = 3,        /* a CUDA runtime call failed; dp_last_error() names it */
-  DP_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait (device-side, in state.error) */
+  DP_ERR_TIMEOUT = 4,     /* a kernel gave up a bounded wait (device-side, in state.error) */
+  DP_ERR_IO = 5           /* a checkpoint file could not be written, read or verified */
 } dp_status_t;
 
 /* Reduction arithmetic.  Both follow the same fixed order (see dp_step). */
@@ -345,6 +346,71 @@ dp_status_t dp_selftest_wait_timeout(dp_step_state_t* d_state, uint64_t timeout_
 dp_status_t dp_step_static(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
                            const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
                            float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream);
+
+/* ---- sharded checkpoints ------------------------------------------------------ */
+
+/* A checkpoint of the optimizer state, stored by shard, that loads into any
+ * layout of the same psi: another n, another stage, other segments.
+ * ("Distributed Training: Split along the Four Axes", checkpoint paragraphs:
+ * ZeRO/FSDP state is saved in shards per rank; a restart either reshards to
+ * the new world size or refuses; the write is temporary files plus an atomic
+ * manifest; the loss scale and the parallel layout are saved with it.)
+ *
+ * On disk, under root/:
+ *   <tag>/shard_<r>.bin  rank r's master, m and v, each dp_shard_len(layout, r)
+ *                        fp32 values in local order (holes of the local space
+ *                        as zeros), after a 24-byte header
+ *   <tag>/state.bin      the dp_step_state_t: t, beta powers, error, loss scale,
+ *                        good_steps; the per-step and kernel fields cleared
+ *   <tag>/layout.bin     the layout it was saved with
+ *   <tag>/user.bin       the caller's bytes (LR schedule, RNG, data cursor ...)
+ *   <tag>/MANIFEST       each file's size and FNV-1a 64-bit checksum
+ *   LATEST               the tag of the newest complete checkpoint
+ * dp_checkpoint_save writes <tag>.partial/, syncs every file, renames it to
+ * <tag>/ and then replaces LATEST by a rename, so a reader sees either the old
+ * or the new checkpoint, never part of one.  A save that fails leaves
+ * <tag>.partial/ behind (a later save of the same tag overwrites it) and
+ * LATEST unchanged.
+ *
+ * master/m/v: arrays of n pointers laid out as for dp_step (stage 0: full
+ * length on every rank, rank r's segments are saved from rank r's copy;
+ * stages 1-3: shard arrays).  host_buffers = 0: they and d_state are device
+ * memory; the call synchronises `stream` first, then copies through a pinned
+ * host chunk on `stream` and returns when all copies are done.
+ * host_buffers = 1: they are host memory and no CUDA call is made.
+ * For dp_step_single_pass, pass the current set (state.cur_set); the loaded
+ * state has cur_set = 0, so load into set 0.
+ * Errors: DP_ERR_INVALID_ARG (bad layout, tag, NULL pointers; nothing
+ * written), DP_ERR_IO (with dp_last_error() naming the file), DP_ERR_CUDA.
+ * tag: 1..200 characters of [A-Za-z0-9_.-], not starting with '.'; an
+ * existing <tag>/ is an error. */
+dp_status_t dp_checkpoint_save(const char* root, const char* tag, const dp_layout_t* layout,
+                               float* const* master, float* const* m, float* const* v,
+                               const dp_step_state_t* d_state, const void* user_meta, uint64_t user_meta_bytes,
+                               int32_t host_buffers, dp_stream_t stream);
+
+/* Loads the checkpoint `tag` (NULL: the one LATEST names) into `layout`,
+ * which must have the saved psi and may differ in everything else.  Every
+ * element lands at its global position's place in the new layout, so the
+ * result is a bit-exact permutation of what was saved.  verify = 1 checks
+ * every file against the manifest first (reads the checkpoint twice).
+ * user_meta_bytes: NULL to skip the user bytes; else in: the capacity of
+ * user_meta, out: the saved size (with user_meta NULL only the size is
+ * returned).  Errors as for dp_checkpoint_save; DP_ERR_INVALID_ARG also for
+ * a psi mismatch or a too-small user_meta.  On an error the destination may
+ * be partly written. */
+dp_status_t dp_checkpoint_load(const char* root, const char* tag, const dp_layout_t* layout,
+                               float* const* master, float* const* m, float* const* v, dp_step_state_t* d_state,
+                               void* user_meta, uint64_t* user_meta_bytes, int32_t host_buffers, int32_t verify,
+                               dp_stream_t stream);
+
+/* The saved layout of checkpoint `tag` (NULL: LATEST) and the size of its
+ * user bytes: any output may be NULL; seg receives the nseg segments if
+ * seg_cap is large enough (else DP_ERR_INVALID_ARG).  verify as for
+ * dp_checkpoint_load.  Reads no shard data unless verify is set. */
+dp_status_t dp_checkpoint_info(const char* root, const char* tag, int32_t verify, int32_t* stage, int32_t* n,
+                               int64_t* psi, int32_t* nseg, dp_segment_t* seg, int32_t seg_cap,
+                               uint64_t* user_meta_bytes);
 
 #ifdef __cplusplus
 }

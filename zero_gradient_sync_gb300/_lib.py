@@ -14,7 +14,7 @@ from typing import List, Optional, Sequence, Tuple
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libdpstep.so")
 
-DP_OK, DP_ERR_INVALID_ARG, DP_ERR_ALIGNMENT, DP_ERR_CUDA, DP_ERR_TIMEOUT = 0, 1, 2, 3, 4
+DP_OK, DP_ERR_INVALID_ARG, DP_ERR_ALIGNMENT, DP_ERR_CUDA, DP_ERR_TIMEOUT, DP_ERR_IO = 0, 1, 2, 3, 4, 5
 DP_SUM_COMPENSATED, DP_SUM_PLAIN = 0, 1
 DP_MAX_N, DP_MAX_NA, DP_MAX_SEG = 16, 64, 1024
 STATE_BYTES = 64
@@ -90,6 +90,12 @@ def _load() -> ctypes.CDLL:
                                         c_vp, c_vp]),
         "dp_step_static": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32,
                                    c_vp, c_vp]),
+        "dp_checkpoint_save": (c_i32, [ctypes.c_char_p, ctypes.c_char_p, P(dp_layout_t), c_vp, c_vp, c_vp, c_vp, c_vp,
+                                       c_u64, c_i32, c_vp]),
+        "dp_checkpoint_load": (c_i32, [ctypes.c_char_p, ctypes.c_char_p, P(dp_layout_t), c_vp, c_vp, c_vp, c_vp, c_vp,
+                                       P(c_u64), c_i32, c_i32, c_vp]),
+        "dp_checkpoint_info": (c_i32, [ctypes.c_char_p, ctypes.c_char_p, c_i32, P(c_i32), P(c_i32), P(c_i64),
+                                       P(c_i32), P(dp_segment_t), c_i32, P(c_u64)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -384,3 +390,86 @@ def read_state(state) -> dict:
     return {"t": s.t, "found_inf": s.found_inf, "error": s.error, "nonfinite": s.nonfinite, "b1t": s.b1t,
             "b2t": s.b2t, "work_count": s.work_count, "work_found": s.work_found, "work_ticket": s.work_ticket,
             "good_steps": s.good_steps, "loss_scale": s.loss_scale, "cur_set": s.cur_set}
+
+
+# ------------------------------------------------------------------------------------------- checkpoints
+
+def _host_addr(x) -> Optional[int]:
+    """Host address of a numpy array / CPU tensor / bytearray, or None if x is a CUDA tensor."""
+    if x is None:
+        return 0
+    if hasattr(x, "is_cuda"):
+        if x.is_cuda:
+            return None
+        if not x.is_contiguous():
+            raise ValueError("checkpoint buffers must be contiguous")
+        return x.data_ptr()
+    if isinstance(x, bytearray):
+        return ctypes.addressof(ctypes.c_char.from_buffer(x))
+    if not x.flags["C_CONTIGUOUS"] or not x.flags["WRITEABLE"]:
+        raise ValueError("checkpoint buffers must be contiguous and writable")
+    return x.ctypes.data
+
+
+def _ckpt_buffers(layout: Layout, master, m, v, state):
+    """Pointer arrays and the host_buffers flag: every buffer on the host, or every buffer a CUDA tensor."""
+    lens = layout.state_lens()
+    for name, ts in (("master", master), ("m", m), ("v", v)):
+        if len(ts) != layout.n:
+            raise ValueError("%s: %d arrays for n = %d" % (name, len(ts), layout.n))
+    items = list(master) + list(m) + list(v) + [state]
+    host = [_host_addr(x) for x in items]
+    if all(h is None for h in host):
+        for name, ts in (("master", master), ("m", m), ("v", v)):
+            _check_tensors(ts, 4, lens, name)
+        return _ptr_array(master), _ptr_array(m), _ptr_array(v), _ptr(state), 0
+    if any(h is None for h in host):
+        raise ValueError("checkpoint buffers must be all on the host or all CUDA tensors")
+    for name, ts in (("master", master), ("m", m), ("v", v)):
+        for r, x in enumerate(ts):
+            nbytes = x.numel() * x.element_size() if hasattr(x, "numel") else x.nbytes
+            if nbytes < 4 * lens[r]:
+                raise ValueError("%s[%d]: %d bytes, need %d" % (name, r, nbytes, 4 * lens[r]))
+    k = layout.n
+    mk = lambda hs: (c_vp * max(1, k))(*hs)
+    return mk(host[:k]), mk(host[k:2 * k]), mk(host[2 * k:3 * k]), host[3 * k], 1
+
+
+def dp_checkpoint_save(root: str, tag: str, layout: Layout, master, m, v, state, user_meta: bytes = b"",
+                       stream=None) -> None:
+    """Saves master/m/v (CUDA tensors, or host arrays: numpy / CPU tensors) and the state by shard."""
+    pm, pmm, pv, ps, host = _ckpt_buffers(layout, master, m, v, state)
+    meta = bytes(user_meta)
+    buf = ctypes.create_string_buffer(meta, max(1, len(meta)))
+    _check(LIB.dp_checkpoint_save(os.fsencode(root), tag.encode(), ctypes.byref(layout.c), pm, pmm, pv, ps,
+                                  buf if meta else None, len(meta), host, 0 if host else _stream(stream)),
+           "dp_checkpoint_save")
+
+
+def dp_checkpoint_load(root: str, tag: Optional[str], layout: Layout, master, m, v, state, verify: bool = True,
+                       stream=None) -> bytes:
+    """Loads checkpoint `tag` (None: LATEST) into `layout`, resharding; returns the saved user bytes."""
+    pm, pmm, pv, ps, host = _ckpt_buffers(layout, master, m, v, state)
+    tb = tag.encode() if tag is not None else None
+    size = c_u64(0)
+    _check(LIB.dp_checkpoint_info(os.fsencode(root), tb, 0, None, None, None, None, None, 0, ctypes.byref(size)),
+           "dp_checkpoint_load")
+    buf = ctypes.create_string_buffer(max(1, size.value))
+    cap = c_u64(size.value)
+    _check(LIB.dp_checkpoint_load(os.fsencode(root), tb, ctypes.byref(layout.c), pm, pmm, pv, ps, buf,
+                                  ctypes.byref(cap), host, int(verify), 0 if host else _stream(stream)),
+           "dp_checkpoint_load")
+    return buf.raw[:cap.value]
+
+
+def dp_checkpoint_info(root: str, tag: Optional[str] = None, verify: bool = False) -> Layout:
+    """The layout checkpoint `tag` (None: LATEST) was saved with."""
+    tb = tag.encode() if tag is not None else None
+    stage, n, nseg, psi = c_i32(0), c_i32(0), c_i32(0), c_i64(0)
+    _check(LIB.dp_checkpoint_info(os.fsencode(root), tb, int(verify), ctypes.byref(stage), ctypes.byref(n),
+                                  ctypes.byref(psi), ctypes.byref(nseg), None, 0, None), "dp_checkpoint_info")
+    arr = (dp_segment_t * max(1, nseg.value))()
+    _check(LIB.dp_checkpoint_info(os.fsencode(root), tb, 0, None, None, None, None, arr, nseg.value, None),
+           "dp_checkpoint_info")
+    return Layout(stage.value, n.value, psi.value,
+                  [(arr[k].global_off, arr[k].len, arr[k].owner, arr[k].local_off) for k in range(nseg.value)])

@@ -210,6 +210,7 @@ const char* dp_status_str(dp_status_t s) {
     case DP_ERR_ALIGNMENT: return "DP_ERR_ALIGNMENT";
     case DP_ERR_CUDA: return "DP_ERR_CUDA";
     case DP_ERR_TIMEOUT: return "DP_ERR_TIMEOUT";
+    case DP_ERR_IO: return "DP_ERR_IO";
   }
   return "DP_ERR_UNKNOWN";
 }
