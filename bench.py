@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--checkpoint", default="",
                    help="time sharded checkpoint save / reshard-load of the workload's optimizer state under this "
                         "directory instead of the step (prints its own JSON line)")
+    p.add_argument("--order", choices=["ring", "tree"], default="ring",
+                   help="order of the ranks' sums: the ring reduce-scatter's, or a binomial tree's")
     p.add_argument("--path", choices=["two-pass", "single-pass"], default="two-pass",
                    help="dp_step (reduce + update kernels) or dp_step_single_pass (one pass, two state sets)")
     return p.parse_args()
@@ -98,9 +100,13 @@ def step_bytes(wl):
     return b1, b1 + 8, 2 * wl.n * wl.a + 4, 4 + 24 + 2 * wl.n
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {"reduce": ("dp_kernels.cu", "dp_device.cuh"), "update": ("dp_kernels.cu", "dp_device.cuh"),
+                  "single_pass": ("dp_kernels.cu", "dp_device.cuh"), "reduce_tree": ("dp_tree.cu", "dp_device.cuh")}
+
+
+def kernel_source_hash(kernel="reduce"):
     h = hashlib.sha256()
-    for f in ("dp_kernels.cu", "dp_device.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "zero_gradient_sync_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -113,7 +119,7 @@ def recorded_traffic(workload, kernel):
         with open(path) as f:
             j = json.load(f)
         e = j[workload][kernel]
-        if e.get("source_hash") != kernel_source_hash():
+        if e.get("source_hash") != kernel_source_hash(kernel):
             return None
         return float(e["bytes_per_launch"])
     except Exception:
@@ -256,7 +262,8 @@ def reference_main(args, wl):
 def config_of(wl, args):
     b1, b2, _, _ = step_bytes(wl)
     return {"workload": wl.description, "psi": wl.psi, "n": wl.n, "a": wl.a, "zero_stage": wl.stage,
-            "layout": wl.layout, "loss_scale": wl.loss_scale, "sum_mode": args.sum, "path": args.path,
+            "layout": wl.layout, "loss_scale": wl.loss_scale, "sum_mode": args.sum, "order": args.order,
+            "path": args.path,
             "grad_dtype": "bf16",
             "state_dtype": "fp32", "bytes_per_param_single_pass": b1, "bytes_per_param_two_pass": b2,
             "l2": "inputs larger than L2: %.1f GB streamed per step vs 129 MB L2, no flush" % (
@@ -283,6 +290,11 @@ def native_main(args, wl):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     mode = dp.DP_SUM_COMPENSATED if args.sum == "compensated" else dp.DP_SUM_PLAIN
+    tree = args.order == "tree"
+    if tree:
+        if args.path == "single-pass":
+            raise SystemExit("--order tree runs on the two-pass path only")
+        mode |= dp.DP_ORDER_TREE
     segs = synth.layout_of(wl)
     layout = dp.Layout(wl.stage, wl.n, wl.psi, segs)
     single = args.path == "single-pass"
@@ -363,7 +375,7 @@ def native_main(args, wl):
     red_ach = red_bytes * wl.psi / (red_avg * 1e-3) / 1e9
     upd_ach = upd_bytes * wl.psi / max(1e-9, upd_avg * 1e-3) / 1e9
     step_gbs = (b1 if single else b2) * wl.psi / (ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name, "single_pass" if single else "reduce")
+    traffic = recorded_traffic(wl.name, "single_pass" if single else ("reduce_tree" if tree else "reduce"))
 
     # End to end through the public call with host buffers: the step's gradients copied from pinned host
     # memory, the step, and the step's status read back, every step.
@@ -419,6 +431,7 @@ def native_main(args, wl):
             "hbm_peak_kind": peak_kind,
             "roofline": {"bound": "hbm",
                          "kernel": ("single-pass reduce + Adam + all-gather" if single else
+                                    "reduce (accumulate + tree reduce + average + check)" if tree else
                                     "reduce (accumulate + ring reduce-scatter + average + check)"),
                          "achieved": red_ach, "peak": peak, "unit": "GB/s", "frac": red_ach / peak,
                          "traffic": traffic, "bytes_per_launch": red_bytes * wl.psi, "avg_ms": red_avg,

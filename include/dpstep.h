@@ -72,11 +72,27 @@ typedef enum {
   DP_ERR_IO = 5           /* a checkpoint file could not be written, read or verified */
 } dp_status_t;
 
-/* Reduction arithmetic.  Both follow the same fixed order (see dp_step). */
+/* Reduction arithmetic, the low 4 bits of every sum_mode argument. */
 enum {
   DP_SUM_COMPENSATED = 0, /* fp32 with Knuth's TwoSum error terms carried alongside */
   DP_SUM_PLAIN = 1        /* plain fp32 additions */
 };
+
+/* Order in which the ranks' sums are added, OR'd into sum_mode
+ * (e.g. DP_SUM_PLAIN | DP_ORDER_TREE).  Both orders are fixed, so results are
+ * bit-identical run to run; they differ from each other by rounding only.
+ *   DP_ORDER_RING: for the chunk owned by s, g_{s+1} + g_{s+2} + ... + g_s
+ *     left to right (the ring reduce-scatter's hops, "Data vs Tensor vs
+ *     Pipeline Parallelism", data parallelism section).
+ *   DP_ORDER_TREE: a binomial tree over rank index rooted at rank 0, the same
+ *     for every element: level l adds the block of ranks
+ *     [j 2^(l+1) + 2^l, (j+1) 2^(l+1)) into [j 2^(l+1), j 2^(l+1) + 2^l), the
+ *     lower block on the left; a block without a partner (n not a power of
+ *     two) moves up a level unchanged.  Compensated: (H, e) = TwoSum(H_left,
+ *     H_right), L = (L_left + e) + L_right.  (NCCL's tree algorithms, named on
+ *     the same page beside the ring for their 2 log2(n) instead of 2(n-1)
+ *     steps.)  dp_step_single_pass takes the ring order only. */
+enum { DP_ORDER_RING = 0, DP_ORDER_TREE = 16 };
 
 /* ZeRO stages of the layout. */
 enum { DP_STAGE_DP = 0, DP_STAGE_ZERO1 = 1, DP_STAGE_ZERO2 = 2, DP_STAGE_ZERO3 = 3 };
@@ -229,7 +245,8 @@ dp_status_t dp_accumulate(float* const* acc, const uint16_t* const* g, int64_t p
  * segment (owner s) and element i in it:
  *   p = acc_{s+1} + acc_{s+2} + ... + acc_s   (ring order: the chunk starts at
  *       rank s+1 and reaches its owner after n-1 hops; compensated mode adds
- *       (hi, lo) pairs with TwoSum and ends with hi + lo)
+ *       (hi, lo) pairs with TwoSum and ends with hi + lo; with DP_ORDER_TREE
+ *       the acc_r are added in the tree order instead)
  *   gbar_shard[s][local_off + (i - global_off)] = fl32(p * fl32(1 / (n S)))
  * then state.found_inf / state.nonfinite report whether any gbar is inf/NaN.
  * gbar_shard[s]: device, dp_shard_len(layout, s) floats.  loss_scale S > 0. */
@@ -255,9 +272,10 @@ dp_status_t dp_allgather_params(uint16_t* const* replicas, const float* const* m
  * grads: host array of n*a device pointers, rank-major (grads[r*a + k] is
  * micro-step k of rank r), each psi bf16.  Per element the gradient is summed
  * in a fixed order -- micro-steps k = 0..a-1 within each rank, then ranks in
- * ring order s+1, ..., s for the owner s -- so results are bit-identical run to
- * run and identical to dp_accumulate + dp_reduce_scatter_avg + dp_adam_shard +
- * dp_allgather_params.  gbar_shard: n device shards of dp_shard_len floats, or
+ * ring order s+1, ..., s for the owner s (or in the tree order of
+ * DP_ORDER_TREE) -- so results are bit-identical run to run and identical to
+ * dp_accumulate + dp_reduce_scatter_avg + dp_adam_shard + dp_allgather_params
+ * with the same sum_mode.  gbar_shard: n device shards of dp_shard_len floats, or
  * NULL to carve them from ws (dp_workspace_size bytes, 256-byte aligned).
  * If any reduced value is not finite (or a wait timed out) master, m, v,
  * replicas and t are left bit-for-bit unchanged. */

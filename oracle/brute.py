@@ -10,6 +10,8 @@
   micro-step), in float32 or float32 (hi, lo) pairs.  This is the reduction
   order the GPU path promises, derived from message passing rather than from
   the GPU code.
+* tree_gbar: the same local accumulation, then the ranks' sums added up the
+  simulated binomial tree of tree.py (the second reduction order).
 """
 from __future__ import annotations
 
@@ -81,3 +83,16 @@ def ring_gbar(grads: Sequence[np.ndarray], n: int, a: int, segs, psi: int, loss_
             p = np.asarray(red[s], dtype=np.float32)
         ring._put(out, s, (p * inv).astype(np.float32))
     return out
+
+
+def tree_gbar(grads: Sequence[np.ndarray], n: int, a: int, segs, psi: int, loss_scale: float,
+              arith: str = "f32") -> np.ndarray:
+    """gbar as the binomial tree (tree.py) computes it after the same rank-local accumulation: float32
+    partials ("f32") or float32 (hi, lo) pairs ("f32pair"), then hi + lo, then one multiply by
+    fl32(1 / (n S)).  The tree's root holds the whole sum; the owner keeps its shard of it."""
+    from .tree import Tree, combine
+    loc = local_accumulate(grads, n, a, arith)
+    tot = Tree(n).reduce(loc, combine(arith), elems=psi)
+    p = (tot[0] + tot[1]).astype(np.float32) if arith == "f32pair" else np.asarray(tot, dtype=np.float32)
+    inv = np.float32(1.0 / (float(n) * float(np.float32(loss_scale))))
+    return (p * inv).astype(np.float32)

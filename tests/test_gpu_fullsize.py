@@ -96,7 +96,7 @@ def warm_state_by_oracle(b, wl, segs):
     b.state.copy_(torch.frombuffer(bytearray(gu.state_bytes(1, wl.beta1, wl.beta2)), dtype=torch.uint8))
 
 
-def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0):
+def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0, mode=dp.DP_SUM_COMPENSATED):
     segs = synth.layout_of(wl)
     L = dp.Layout(wl.stage, wl.n, wl.psi, segs)
     b = StepBuffers(L, wl.a)
@@ -108,7 +108,7 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0):
     else:
         sd.fill_master(b.master, wl, segs, wl.stage)
     A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
-    b.reduce(A, wl.loss_scale, dp.DP_SUM_COMPENSATED)
+    b.reduce(A, wl.loss_scale, mode)
     b.update(A)
     torch.cuda.synchronize()
     st = dp.read_state(b.state)
@@ -134,7 +134,7 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0):
         # the fixed-order reduction is bit-identical run to run over the whole parameter space
         first = [x.clone() for x in b.gbar]
         for _ in range(repeat):
-            b.reduce(A, wl.loss_scale, dp.DP_SUM_COMPENSATED)
+            b.reduce(A, wl.loss_scale, mode)
             torch.cuda.synchronize()
             for x, y in zip(first, b.gbar):
                 assert torch.equal(x.view(torch.int32), y.view(torch.int32))
@@ -146,7 +146,7 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0):
         b.grad(r, k)[i:i + 1].view(torch.int16).fill_(synth.BF16_POS_INF)
         before = [gather_state(x, segs, idx, wl.stage) for x in (b.master, b.m, b.v)]
         reps_before = [sd.bits_of_bf16(x[gi]) for x in b.replicas]
-        b.reduce(A, wl.loss_scale, dp.DP_SUM_COMPENSATED)
+        b.reduce(A, wl.loss_scale, mode)
         b.update(A)
         torch.cuda.synchronize()
         st2 = dp.read_state(b.state)
@@ -164,6 +164,12 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0):
 def test_fullsize_gpt2_small(dev):
     """123,568,896 params, n=8, a=4, ZeRO-1 even, loss scale 2^16: the benchmark's workload."""
     run_fullsize(synth.WORKLOADS["gpt2_small"], inject=True, repeat=3)
+
+
+def test_fullsize_gpt2_small_tree_order(dev):
+    """The benchmark's workload with the ranks' sums added up the binomial tree instead of the ring."""
+    run_fullsize(synth.WORKLOADS["gpt2_small"], inject=True, repeat=2,
+                 mode=dp.DP_SUM_COMPENSATED | dp.DP_ORDER_TREE)
 
 
 def test_fullsize_gpt_1p3b(dev):

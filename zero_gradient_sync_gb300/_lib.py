@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(HERE, "libdpstep.so")
 
 DP_OK, DP_ERR_INVALID_ARG, DP_ERR_ALIGNMENT, DP_ERR_CUDA, DP_ERR_TIMEOUT, DP_ERR_IO = 0, 1, 2, 3, 4, 5
 DP_SUM_COMPENSATED, DP_SUM_PLAIN = 0, 1
+DP_ORDER_RING, DP_ORDER_TREE = 0, 16   # OR'd into sum_mode
 DP_MAX_N, DP_MAX_NA, DP_MAX_SEG = 16, 64, 1024
 STATE_BYTES = 64
 

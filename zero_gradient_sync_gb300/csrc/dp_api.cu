@@ -129,9 +129,16 @@ dp_status_t check_adam(const dp_adam_t& A) {
   return DP_OK;
 }
 
+// sum_mode = arithmetic (DP_SUM_*) | rank order (DP_ORDER_*).
+static bool split_mode(int sum_mode, int& arith, int& order) {
+  arith = sum_mode & 0xF;
+  order = sum_mode & ~0xF;
+  return (arith == DP_SUM_COMPENSATED || arith == DP_SUM_PLAIN) && (order == DP_ORDER_RING || order == DP_ORDER_TREE);
+}
+
 dp_status_t scalars(const Plan& P, const dp_adam_t* A, float loss_scale, int sum_mode, StepScalars& s) {
-  if (sum_mode != DP_SUM_COMPENSATED && sum_mode != DP_SUM_PLAIN)
-    return fail(DP_ERR_INVALID_ARG, "sum_mode %d unknown", sum_mode);
+  int arith = 0, order = 0;
+  if (!split_mode(sum_mode, arith, order)) return fail(DP_ERR_INVALID_ARG, "sum_mode %d unknown", sum_mode);
   if (!std::isfinite(loss_scale) || !(loss_scale > 0.0f))
     return fail(DP_ERR_INVALID_ARG, "loss scale must be finite and > 0");
   const double inv = 1.0 / ((double)P.n * (double)loss_scale);
@@ -139,7 +146,8 @@ dp_status_t scalars(const Plan& P, const dp_adam_t* A, float loss_scale, int sum
   if (!std::isfinite(inv32) || !(inv32 >= 1.17549435e-38f))
     return fail(DP_ERR_INVALID_ARG, "1 / (n * loss_scale) is not a normal fp32 number");
   s.inv = inv32;
-  s.mode = sum_mode;
+  s.mode = arith;
+  s.order = order;
   s.timeout_ns = g_timeout_ns.load();
   s.scaler = dp::ScalerK{0, 1, 1.0f, 1.0f, 1.0f, 1.0f};
   if (A) {
@@ -272,7 +280,7 @@ size_t dp_workspace_size(const dp_layout_t* layout) {
 
 size_t dp_acc_elems(int64_t psi, int32_t sum_mode) {
   if (psi < 0) return 0;
-  return (size_t)psi * (sum_mode == DP_SUM_COMPENSATED ? 2u : 1u);
+  return (size_t)psi * ((sum_mode & 0xF) == DP_SUM_COMPENSATED ? 2u : 1u);
 }
 
 int64_t dp_global_batch(int64_t b, int32_t n, int32_t a) {
@@ -338,14 +346,14 @@ dp_status_t dp_state_init(dp_step_state_t* d_state, dp_stream_t stream) {
 dp_status_t dp_accumulate(float* const* acc, const uint16_t* const* g, int64_t psi, int32_t n, int32_t first,
                           int32_t sum_mode, dp_stream_t stream) {
   if (psi < 0 || n < 1 || n > DP_MAX_N) return fail(DP_ERR_INVALID_ARG, "bad psi or n");
-  if (sum_mode != DP_SUM_COMPENSATED && sum_mode != DP_SUM_PLAIN)
-    return fail(DP_ERR_INVALID_ARG, "sum_mode %d unknown", sum_mode);
+  int arith = 0, order = 0;  // the rank order plays no part in a rank's own accumulation
+  if (!split_mode(sum_mode, arith, order)) return fail(DP_ERR_INVALID_ARG, "sum_mode %d unknown", sum_mode);
   dp_status_t st = check_ptr_array((const void* const*)acc, n, "acc");
   if (st == DP_OK) st = check_ptr_array((const void* const*)g, n, "g");
   if (st != DP_OK) return st;
   if (psi == 0) return DP_OK;
   LaunchCount lc;
-  cudaError_t e = dp::launch_accumulate(acc, g, psi, n, first, sum_mode, (cudaStream_t)stream, &lc.n);
+  cudaError_t e = dp::launch_accumulate(acc, g, psi, n, first, arith, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "accumulate launch");
 }
 
@@ -360,7 +368,9 @@ dp_status_t dp_reduce_scatter_avg(float* const* gbar_shard, const float* const* 
   if ((st = check_full_arrays(P, (const void* const*)acc, P.n, "acc")) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
-  cudaError_t e = dp::launch_rs_avg(P, acc, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n);
+  cudaError_t e = s.order == DP_ORDER_TREE
+                      ? dp::launch_rs_tree(P, acc, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n)
+                      : dp::launch_rs_avg(P, acc, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "reduce_scatter_avg launch");
 }
 
@@ -411,6 +421,13 @@ static dp_status_t prepare_reduce(const Plan& P, const uint16_t* const* grads, i
   return st;
 }
 
+// Pass A in the order s names.
+static cudaError_t launch_pass_a(const Plan& P, const uint16_t* const* grads, int a, float* const* gb,
+                                 const StepScalars& s, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  if (s.order == DP_ORDER_TREE) return dp::launch_reduce_tree(P, grads, a, gb, s, 1, st, stream, launches);
+  return dp::launch_reduce(P, grads, a, gb, s, 1, st, stream, launches);
+}
+
 dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* const* grads, int32_t a,
                            const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
                            dp_step_state_t* d_state, dp_stream_t stream) {
@@ -422,7 +439,7 @@ dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* c
   if ((st = prepare_reduce(P, grads, a, adam, loss_scale, sum_mode, gbar_shard, ws, d_state, s, gb)) != DP_OK)
     return st;
   LaunchCount lc;
-  cudaError_t e = dp::launch_reduce(P, grads, a, gb, s, 1, d_state, (cudaStream_t)stream, &lc.n);
+  cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "reduce launch");
 }
 
@@ -458,7 +475,7 @@ dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* cons
   if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
   if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
   LaunchCount lc;
-  cudaError_t e = dp::launch_reduce(P, grads, a, gb, s, 1, d_state, (cudaStream_t)stream, &lc.n);
+  cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
   e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
@@ -496,7 +513,7 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
   if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
   s.scaler = dp::ScalerK{1, c.growth_interval, c.growth_factor, c.backoff_factor, c.min_scale, c.max_scale};
   LaunchCount lc;
-  cudaError_t e = dp::launch_reduce(P, grads, a, gb, s, 1, d_state, (cudaStream_t)stream, &lc.n);
+  cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
   e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
@@ -513,6 +530,7 @@ dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master,
     return fail(DP_ERR_INVALID_ARG, "a = %d: need 1 <= a and n * a <= %d", a, DP_MAX_NA);
   StepScalars s;
   if ((st = scalars(P, &adam, loss_scale, sum_mode, s)) != DP_OK) return st;
+  if (s.order != DP_ORDER_RING) return fail(DP_ERR_INVALID_ARG, "dp_step_single_pass: ring order only");
   if ((st = check_full_arrays(P, (const void* const*)grads, P.n * a, "grads")) != DP_OK) return st;
   if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
   int64_t lens2[2 * DP_MAX_N];

@@ -541,13 +541,24 @@ bool open_checkpoint(const char* root, const char* tag, int verify, std::string&
   if (!read_manifest(dir, man, err)) return false;
   if (!read_layout(dir, old, old_segs, err)) return false;
   if (old.n < 1 || old.n > DP_MAX_N) return err.set(DP_ERR_IO, "checkpoint: saved layout has a bad n");
+  std::vector<const ManifestEntry*> ents;
   for (const std::string& name : required_files(old.n)) {
     const ManifestEntry* e = nullptr;
     for (const ManifestEntry& x : man)
       if (x.name == name) e = &x;
     if (!e) return err.set(DP_ERR_IO, "checkpoint: manifest of " + dir + " lacks " + name);
-    if (verify && !verify_file(dir + "/" + name, *e, err)) return false;
     if (name == "user.bin" && user_bytes) *user_bytes = e->bytes;
+    ents.push_back(e);
+  }
+  if (verify) {
+    // one file per work item: the checksum chain is sequential within a file
+    Err v = parallel_items((int64_t)ents.size(), io_workers(), [&](int64_t i, int, Err& e) {
+      return verify_file(dir + "/" + ents[i]->name, *ents[i], e);
+    });
+    if (v.code != DP_OK) {
+      err = v;
+      return false;
+    }
   }
   return true;
 }

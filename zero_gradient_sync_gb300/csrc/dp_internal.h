@@ -25,7 +25,8 @@ struct Plan {
 struct StepScalars {
   float lr, beta1, beta2, eps, omb1, omb2;
   float inv;  // fl32(1 / (n S))
-  int32_t mode;
+  int32_t mode;   // DP_SUM_COMPENSATED or DP_SUM_PLAIN
+  int32_t order;  // DP_ORDER_RING or DP_ORDER_TREE
   uint64_t timeout_ns;
   ScalerK scaler;  // disabled unless the step uses the device-resident loss scale
 };
@@ -36,6 +37,12 @@ dp_status_t report_error(dp_status_t s, const char* msg);
 // Each launcher returns the launch's cudaError_t and adds to *launches.
 cudaError_t launch_reduce(const Plan& P, const uint16_t* const* g, int a, float* const* gbar, const StepScalars& s,
                           int advance, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+// Tree order (dp_tree.cu): pass A and the staged reduce-scatter.
+cudaError_t launch_reduce_tree(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
+                               const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream,
+                               uint64_t* launches);
+cudaError_t launch_rs_tree(const Plan& P, const float* const* acc, float* const* gbar, const StepScalars& s,
+                           dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
 cudaError_t launch_single_pass(const Plan& P, const uint16_t* const* g, int a, uint16_t* const* rep,
                                float* const* master2, float* const* m2, float* const* v2, const StepScalars& s,
                                dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
