@@ -67,7 +67,7 @@ def test_tree_step_matches_oracle(dev, psi, n, a, stage, layout, extra):
 
 def test_tree_on_the_tiny_workload_and_loss_scale_one(dev):
     """The 2^20-parameter, n=2 workload, and a loss-scale-1 cold start with outliers, compensated tree."""
-    for wl in (BASE, BASE.with_(psi=300_007, n=6, a=2, loss_scale=1.0, outlier_p=0.01, seed=9)):
+    for wl in (BASE, BASE.with_(psi=300_007, n=6, a=2, loss_scale=1.0, tail_p=0.01, tail_mult=100.0, seed=9)):
         c = gu.make_case(wl)
         b = gu.upload(c)
         b.step(adam_of(wl), wl.loss_scale, COMP | TREE)
