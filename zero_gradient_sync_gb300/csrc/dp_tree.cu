@@ -8,10 +8,11 @@
 // of two) goes up a level unchanged.  The order does not depend on the shard owner (the all-reduce root is
 // rank 0 for every element); each owner keeps its shard of the result.
 //
-// reduce_tree_kernel: each thread reduces 4 consecutive elements of all n*a inputs and keeps the tree as a
-// binary counter: slot l holds the pending sum of a complete block of 2^l ranks, so at most log2(n) + 1
-// partial sums are live, each in registers.  The ring kernel's shared-memory pipeline cannot hold these
-// partials at 16 elements a thread, so this kernel streams with plain 8-byte loads, 8 in flight per thread.
+// reduce_tree_kernel: the ring kernel's stream -- one producer thread issuing 1-D bulk copies of every input
+// into a ring of shared-memory stages, bounded mbarrier waits -- with a consumer that keeps the tree as a
+// binary counter: slot l holds the pending sum of a complete block of 2^l ranks, so at most log2(n) partial
+// sums are live, each in registers.  To leave room for them a consumer thread owns 8 elements (the ring
+// kernel's 16), so a stage holds half a tile (3840 elements, a 7.5 KB copy) and the ring has twice the stages.
 // rs_tree_kernel: the same tree over the staged per-rank accumulators, one element per thread.
 #include "dp_device.cuh"
 #include "dp_internal.h"
@@ -19,15 +20,25 @@
 namespace dp {
 namespace {
 
-constexpr int RT_THREADS = 256;
-constexpr int RT_DEPTH = 8;   // input loads in flight per thread
-constexpr int RT_LEVELS = 5;  // slots for n <= 16 = 2^4: levels 0..4
+constexpr int TT_CWARPS = 15;
+constexpr int TT_CTHREADS = TT_CWARPS * 32;
+constexpr int TT_EPT = 8;                          // elements per consumer thread: one 16-byte shared load
+constexpr int TT_THREADS = TT_CTHREADS + 32;       // + one producer warp
+constexpr int TT_SUB = TT_CTHREADS * TT_EPT;       // elements of a stage: half a tile
+constexpr int TT_STAGES = 24;
+constexpr int TT_STAGE_BYTES = TT_SUB * 2;
+constexpr int TT_SMEM = TT_STAGES * TT_STAGE_BYTES + 2 * TT_STAGES * 8 + 32;
+constexpr int RT_LEVELS = 5;                       // staged kernel: slots for n <= 16 (levels 0..4)
+static_assert(TILE == 2 * TT_SUB, "a tile is two stages");
+static_assert(TT_STAGE_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
+static_assert(TT_SMEM + 64 <= 227 * 1024, "shared memory fits one CTA");
 
 template <int MAXSEG>
 struct TreeParams {
   const uint16_t* g[DP_MAX_NA];
   float* gbar[DP_MAX_N];
   dp_step_state_t* state;
+  uint64_t timeout_ns;
   double beta1, beta2;
   float inv;
   int32_t n, a, advance;
@@ -35,17 +46,17 @@ struct TreeParams {
   SegTable<MAXSEG> seg;
 };
 
-// Four elements' partial sum: packed hi pairs and (compensated) their accumulated rounding errors.
-struct Part4 {
-  f2_t h[2], l[2];
+// Eight elements' partial sum: packed hi pairs and (compensated) their accumulated rounding errors.
+struct Part8 {
+  f2_t h[4], l[4];
 };
 
 // left + right, left being the lower-index block: (H, e) = TwoSum(left.H, right.H), L = (left.L + e) + right.L.
 template <bool COMP>
-__device__ __forceinline__ Part4 tree_add(const Part4& x, const Part4& y) {
-  Part4 z;
+__device__ __forceinline__ Part8 tree_add(const Part8& x, const Part8& y) {
+  Part8 z;
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
+  for (int u = 0; u < 4; ++u) {
     if (COMP) {
       f2_t e;
       z.h[u] = f2_two_sum(x.h[u], y.h[u], e);
@@ -58,134 +69,234 @@ __device__ __forceinline__ Part4 tree_add(const Part4& x, const Part4& y) {
   return z;
 }
 
-// Quad [e, e + 4) of one bf16 input as 4 bf16 in two words; elements at or past psi read as +0.
-__device__ __forceinline__ uint2 load_quad(const uint16_t* src, int64_t e, int64_t psi) {
-  if (e + 4 <= psi) return __ldcs(reinterpret_cast<const uint2*>(src + e));
-  uint32_t w[2] = {0u, 0u};
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-    if (e + u < psi) w[u >> 1] |= (uint32_t)src[e + u] << (16 * (u & 1));
-  return make_uint2(w[0], w[1]);
+struct StagePos {
+  uint32_t slot = 0, phase = 0, count = 0;
+  __device__ __forceinline__ void next() {
+    ++count;
+    if (++slot == TT_STAGES) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// The stage range of half h of a tile: the tile's elements [lo, hi) in that half, copied as the 8-aligned
+// hull [lo & ~7, min(ceil8(hi), psi & ~7)) -- the buffer's last partial 8 elements are read from global.
+struct Half {
+  int64_t lo, hi, sa;
+  __device__ __forceinline__ bool empty() const { return lo >= hi; }
+};
+__device__ __forceinline__ Half half_of(const Tile& t, int h) {
+  const int64_t cb = (t.start / TILE) * TILE + (int64_t)h * TT_SUB;
+  Half x;
+  x.lo = t.start > cb ? t.start : cb;
+  x.hi = t.end < cb + TT_SUB ? t.end : cb + TT_SUB;
+  x.sa = x.lo & ~int64_t(7);
+  return x;
 }
 
-template <int MAXSEG, bool COMP>
-__global__ void __launch_bounds__(RT_THREADS) reduce_tree_kernel(const __grid_constant__ TreeParams<MAXSEG> p) {
-  __shared__ unsigned long long s_count;
+// LEVELS = log2 of the largest n this instance serves (3: n <= 8, 4: n <= 16); slots 0..LEVELS-1 hold
+// pending blocks, and a full block of 2^LEVELS ranks is the total itself.
+template <int MAXSEG, bool COMP, int LEVELS>
+__global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid_constant__ TreeParams<MAXSEG> p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TT_STAGES * TT_STAGE_BYTES);
+  uint64_t* empty = full + TT_STAGES;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + TT_STAGES);
+  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + TT_STAGES + 1);
   __shared__ float s_inv;
-  __shared__ int s_bad_scale;
-  const int tid = threadIdx.x;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = p.n, a = p.a;
+  const int ntiles = p.seg.ntiles;
+  const int64_t psi = p.seg.psi;
+  const int64_t p8 = psi & ~int64_t(7);
+
   if (tid == 0) {
-    s_count = 0ull;
+    for (int s = 0; s < TT_STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), TT_CWARPS);
+    }
+    *s_abort = 0;
+    *s_count = 0ull;
     float inv = p.inv;
-    int bad = 0;
     if (p.scaler.enabled) {
       // fl32(1 / (n S)) from the device-resident scale, as for the ring order.
       const float sc = *reinterpret_cast<volatile const float*>(&p.state->loss_scale);
       inv = (float)(1.0 / ((double)p.n * (double)sc));
       if (!(sc > 0.0f) || nonfinite(sc) || !(inv >= 1.17549435e-38f) || nonfinite(inv)) {
         record_error(p.state, DP_ERR_INVALID_ARG);
-        bad = 1;
+        *s_abort = 1;
         inv = 0.0f;
       }
     }
     s_inv = inv;
-    s_bad_scale = bad;
+    fence_mbar_init();
   }
   __syncthreads();
-  const int n = p.n, a = p.a, na = n * a;
-  const int64_t psi = p.seg.psi;
-  const f2_t inv2 = f2_pack(s_inv, s_inv);
+
   unsigned bad = 0;
-  TileWalker<MAXSEG> walk;
-  for (int tile = s_bad_scale ? p.seg.ntiles : blockIdx.x; tile < p.seg.ntiles; tile += gridDim.x) {
-    const Tile t = walk.at(p.seg, tile);
-    const int64_t A = t.start & ~int64_t(3), B = (t.end + 3) & ~int64_t(3);
-    float* const dst = p.gbar[t.owner] + (t.loff - t.goff);
-    for (int64_t e = A + 4 * (int64_t)tid; e < B; e += 4 * RT_THREADS) {
-      uint2 buf[RT_DEPTH];
+  if (warp == TT_CWARPS) {
+    // ------------------------------------------------------------ producer: inputs in rank order 0..n-1
+    if (lane == 0) {
+      StagePos sp;
+      TileWalker<MAXSEG> walk;
+      for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
+        const Tile t = walk.at(p.seg, tile);
+        for (int h = 0; h < 2 && !*s_abort; ++h) {
+          const Half x = half_of(t, h);
+          if (x.empty()) continue;
+          int64_t sb = (x.hi + 7) & ~int64_t(7);
+          if (sb > p8) sb = p8;
+          const uint32_t bytes = sb > x.sa ? (uint32_t)(sb - x.sa) * 2u : 0u;
+          for (int q = 0; q < n * a && !*s_abort; ++q) {
+            if (sp.count >= (uint32_t)TT_STAGES &&
+                !mbar_wait_bounded(smem_u32(&empty[sp.slot]), sp.phase ^ 1u, p.timeout_ns, s_abort)) {
+              if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+              *s_abort = 1;
+              break;
+            }
+            const uint32_t fb = smem_u32(&full[sp.slot]);
+            mbar_arrive_expect_tx(fb, bytes);
+            if (bytes) bulk_g2s(smem_u32(stages + sp.slot * TT_STAGE_BYTES), p.g[q] + x.sa, bytes, fb);
+            sp.next();
+          }
+        }
+      }
+      // Never leave with copies in flight: wait for the newest issued phase of every slot.
+      if (*s_abort) {
+        const uint32_t it = sp.count;
+        const uint32_t first = it > (uint32_t)TT_STAGES ? it - TT_STAGES : 0u;
+        for (uint32_t y = first; y < it; ++y)
+          (void)mbar_wait_bounded(smem_u32(&full[y % TT_STAGES]), (y / TT_STAGES) & 1u, p.timeout_ns, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumers: 8 elements per thread
+    const f2_t inv2 = f2_pack(s_inv, s_inv);
+    StagePos sp;
+    TileWalker<MAXSEG> walk;
+    bool live = true;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const Tile t = walk.at(p.seg, tile);
+      for (int h = 0; h < 2; ++h) {
+        const Half x = half_of(t, h);
+        if (x.empty()) continue;
+        const int64_t e0 = x.sa + TT_EPT * tid;
+        const bool active = e0 < x.hi;
+        const bool tailgrp = active && (e0 + TT_EPT > p8);
+
+        // One stage: wait for its bytes, take this thread's 8 values, release the slot.
+        auto take = [&](const uint16_t* src, uint32_t (&w)[4]) {
+          if (live && !mbar_wait_bounded(smem_u32(&full[sp.slot]), sp.phase, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+            *s_abort = 1;
+            live = false;
+          }
 #pragma unroll
-      for (int u = 0; u < RT_DEPTH; ++u)
-        if (u < na) buf[u] = load_quad(p.g[u], e, psi);
-      Part4 slot[RT_LEVELS], cur;
-      int r = 0, k = 0;
-      for (int q0 = 0; q0 < na; q0 += RT_DEPTH) {
-#pragma unroll
-        for (int u = 0; u < RT_DEPTH; ++u) {
-          const int q = q0 + u;
-          if (q < na) {
-            const uint2 w = buf[u];
-            if (q + RT_DEPTH < na) buf[u] = load_quad(p.g[q + RT_DEPTH], e, psi);
-            const f2_t x0 = bf16x2_to_f2(w.x), x1 = bf16x2_to_f2(w.y);
-            if (k == 0) {
-              cur.h[0] = x0;
-              cur.h[1] = x1;
-              cur.l[0] = cur.l[1] = 0ull;
-            } else if (COMP) {
-              f2_t e0, e1;
-              cur.h[0] = f2_fast_two_sum(cur.h[0], x0, e0);
-              cur.h[1] = f2_fast_two_sum(cur.h[1], x1, e1);
-              cur.l[0] = f2_add(cur.l[0], e0);
-              cur.l[1] = f2_add(cur.l[1], e1);
+          for (int u = 0; u < 4; ++u) w[u] = 0u;
+          if (active && live) {
+            if (!tailgrp) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stages + sp.slot * TT_STAGE_BYTES + 2 * TT_EPT * tid);
+              w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
             } else {
-              cur.h[0] = f2_add(cur.h[0], x0);
-              cur.h[1] = f2_add(cur.h[1], x1);
-            }
-            if (++k == a) {
-              // Rank r is complete: add it into the counter.  Bit l of r marks an occupied slot l, which
-              // holds the block just below it; merging carries the sum up until a free slot takes it.
-              // The slots below the lowest clear bit of r are all occupied and merge; that bit's slot takes
-              // the sum (static slot indices keep every slot in registers).
-              const int top = __ffs(~r) - 1;
-              Part4 v = cur;
 #pragma unroll
-              for (int lv = 0; lv < RT_LEVELS; ++lv) {
-                if (lv < top) v = tree_add<COMP>(slot[lv], v);
-                else if (lv == top) slot[lv] = v;
+              for (int u = 0; u < TT_EPT; ++u) {
+                const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
+                w[u >> 1] |= (u & 1) ? (b << 16) : b;
               }
-              k = 0;
-              ++r;
+            }
+          }
+          // The slot is refilled by the async proxy: order this thread's reads of it before that write.
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty[sp.slot]));
+          sp.next();
+        };
+
+        Part8 slot[LEVELS], whole, cur;
+        for (int r = 0; r < n; ++r) {
+          uint32_t w[4];
+          take(p.g[r * a], w);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            cur.h[u] = bf16x2_to_f2(w[u]);
+            cur.l[u] = 0ull;
+          }
+          for (int k = 1; k < a; ++k) {
+            take(p.g[r * a + k], w);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const f2_t xx = bf16x2_to_f2(w[u]);
+              if (COMP) {
+                f2_t e;
+                cur.h[u] = f2_fast_two_sum(cur.h[u], xx, e);
+                cur.l[u] = f2_add(cur.l[u], e);
+              } else {
+                cur.h[u] = f2_add(cur.h[u], xx);
+              }
+            }
+          }
+          // Rank r is complete.  The slots below the lowest clear bit of r are all occupied and merge into
+          // it; that bit's slot takes the sum (static slot indices keep every slot in registers).
+          const int top = __ffs(~r) - 1;
+#pragma unroll
+          for (int lv = 0; lv < LEVELS; ++lv) {
+            if (lv < top) cur = tree_add<COMP>(slot[lv], cur);
+            else if (lv == top) slot[lv] = cur;
+          }
+          if (top == LEVELS) whole = cur;
+        }
+        // Blocks left without a partner, smallest first, each joining the one below it on the left.
+        Part8 tot = whole;
+        if (n != (1 << LEVELS)) {
+          bool have = false;
+#pragma unroll
+          for (int lv = 0; lv < LEVELS; ++lv) {
+            if ((n >> lv) & 1) {
+              tot = have ? tree_add<COMP>(slot[lv], tot) : slot[lv];
+              have = true;
             }
           }
         }
-      }
-      // Blocks left without a partner, smallest first, each joining the one below it on the left.
-      Part4 tot = cur;
-      bool have = false;
+        float o[TT_EPT];
 #pragma unroll
-      for (int lv = 0; lv < RT_LEVELS; ++lv) {
-        if ((n >> lv) & 1) {
-          tot = have ? tree_add<COMP>(slot[lv], tot) : slot[lv];
-          have = true;
+        for (int u = 0; u < 4; ++u) {
+          const f2_t pp = COMP ? f2_add(tot.h[u], tot.l[u]) : tot.h[u];
+          f2_unpack(f2_mul(pp, inv2), o[2 * u], o[2 * u + 1]);
         }
-      }
-      float o[4];
+        if (active) {
+          float* dst = p.gbar[t.owner] + (t.loff + (e0 - t.goff));
+          const bool all = e0 >= x.lo && e0 + TT_EPT <= x.hi;
+          if (all && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const f2_t pp = COMP ? f2_add(tot.h[u], tot.l[u]) : tot.h[u];
-        f2_unpack(f2_mul(pp, inv2), o[2 * u], o[2 * u + 1]);
-      }
-      const bool whole = e >= t.start && e + 4 <= t.end;
-      float* d = dst + e;
-      if (whole && ((reinterpret_cast<uintptr_t>(d) & 15) == 0)) {
-        *reinterpret_cast<float4*>(d) = make_float4(o[0], o[1], o[2], o[3]);
-        bad += nonfinite(o[0]) + nonfinite(o[1]) + nonfinite(o[2]) + nonfinite(o[3]);
-      } else {
+            for (int u = 0; u < TT_EPT; ++u) bad += nonfinite(o[u]);
+          } else {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (e + u >= t.start && e + u < t.end) {
-            d[u] = o[u];
-            bad += nonfinite(o[u]);
+            for (int u = 0; u < TT_EPT; ++u)
+              if (e0 + u >= x.lo && e0 + u < x.hi) {
+                dst[u] = o[u];
+                bad += nonfinite(o[u]);
+              }
           }
+        }
       }
     }
   }
+
+  // ------------------------------------------------------------ CTA total, then the grid's
   unsigned long long c = bad;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
-  if ((tid & 31) == 0 && c) atomicAdd(&s_count, c);
+  __syncthreads();
+  if (lane == 0 && c) atomicAdd(s_count, c);
   __syncthreads();
   if (tid == 0)
-    finish_reduction(p.state, s_count, (s_count != 0ull) || s_bad_scale, p.advance, p.beta1, p.beta2, &p.scaler, 0);
+    finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2, &p.scaler, 0);
 }
 
 // ---------------------------------------------------------------- staged: the tree over per-rank accumulators
@@ -285,25 +396,26 @@ void fill_table(SegTable<MAXSEG>& T, const Plan& P) {
 
 // Resident CTAs of `kernel` on every SM, capped by the tile count (at least 1: every CTA joins the finish).
 template <typename K>
-int resident_grid(K kernel, int threads, int ntiles) {
+int resident_grid(K kernel, int threads, size_t smem, int ntiles) {
   int dev = 0, sms = 0, per_sm = 1;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                    cudaSuccess || sms < 1)
     sms = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   long long g = (long long)sms * per_sm;
   if (ntiles < g) g = ntiles;
   return (int)(g < 1 ? 1 : g);
 }
 
-template <int MAXSEG, bool COMP>
+template <int MAXSEG, bool COMP, int LEVELS>
 cudaError_t launch_tree_t(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
                           const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream) {
   TreeParams<MAXSEG> prm;
   for (int q = 0; q < P.n * a; ++q) prm.g[q] = g[q];
   for (int r = 0; r < P.n; ++r) prm.gbar[r] = gbar[r];
   prm.state = st;
+  prm.timeout_ns = s.timeout_ns;
   prm.beta1 = (double)s.beta1;
   prm.beta2 = (double)s.beta2;
   prm.inv = s.inv;
@@ -312,9 +424,27 @@ cudaError_t launch_tree_t(const Plan& P, const uint16_t* const* g, int a, float*
   prm.advance = advance;
   prm.scaler = s.scaler;
   fill_table(prm.seg, P);
-  auto kern = reduce_tree_kernel<MAXSEG, COMP>;
-  kern<<<resident_grid(kern, RT_THREADS, P.ntiles), RT_THREADS, 0, stream>>>(prm);
+  auto kern = reduce_tree_kernel<MAXSEG, COMP, LEVELS>;
+  // The opt-in shared-memory size is set once per device (not inside a stream capture on later calls).
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TT_SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  // One CTA per SM (every CTA joins the grid-wide finish, so at least one runs even with no tiles).
+  kern<<<resident_grid(kern, TT_THREADS, TT_SMEM, P.ntiles), TT_THREADS, TT_SMEM, stream>>>(prm);
   return cudaGetLastError();
+}
+
+template <int MAXSEG, bool COMP>
+cudaError_t launch_tree_n(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
+                          const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream) {
+  if (P.n <= 8) return launch_tree_t<MAXSEG, COMP, 3>(P, g, a, gbar, s, advance, st, stream);
+  return launch_tree_t<MAXSEG, COMP, 4>(P, g, a, gbar, s, advance, st, stream);
 }
 
 template <int MAXSEG, bool COMP>
@@ -330,7 +460,7 @@ cudaError_t launch_rs_tree_t(const Plan& P, const float* const* acc, float* cons
   prm.n = P.n;
   fill_table(prm.seg, P);
   auto kern = rs_tree_kernel<MAXSEG, COMP>;
-  kern<<<resident_grid(kern, 256, P.ntiles), 256, 0, stream>>>(prm);
+  kern<<<resident_grid(kern, 256, 0, P.ntiles), 256, 0, stream>>>(prm);
   return cudaGetLastError();
 }
 
@@ -342,10 +472,10 @@ cudaError_t launch_reduce_tree(const Plan& P, const uint16_t* const* g, int a, f
   ++*launches;
   const bool comp = s.mode == DP_SUM_COMPENSATED;
   if (P.nseg <= SMALL_SEG)
-    return comp ? launch_tree_t<SMALL_SEG, true>(P, g, a, gbar, s, advance, st, stream)
-                : launch_tree_t<SMALL_SEG, false>(P, g, a, gbar, s, advance, st, stream);
-  return comp ? launch_tree_t<BIG_SEG, true>(P, g, a, gbar, s, advance, st, stream)
-              : launch_tree_t<BIG_SEG, false>(P, g, a, gbar, s, advance, st, stream);
+    return comp ? launch_tree_n<SMALL_SEG, true>(P, g, a, gbar, s, advance, st, stream)
+                : launch_tree_n<SMALL_SEG, false>(P, g, a, gbar, s, advance, st, stream);
+  return comp ? launch_tree_n<BIG_SEG, true>(P, g, a, gbar, s, advance, st, stream)
+              : launch_tree_n<BIG_SEG, false>(P, g, a, gbar, s, advance, st, stream);
 }
 
 cudaError_t launch_rs_tree(const Plan& P, const float* const* acc, float* const* gbar, const StepScalars& s,
