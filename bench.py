@@ -49,8 +49,9 @@ def parse():
                         "directory instead of the step (prints its own JSON line)")
     p.add_argument("--order", choices=["ring", "tree"], default="ring",
                    help="order of the ranks' sums: the ring reduce-scatter's, or a binomial tree's")
-    p.add_argument("--path", choices=["two-pass", "single-pass"], default="two-pass",
-                   help="dp_step (reduce + update kernels) or dp_step_single_pass (one pass, two state sets)")
+    p.add_argument("--path", choices=["two-pass", "single-pass", "microstep"], default="two-pass",
+                   help="dp_step (reduce + update kernels), dp_step_single_pass (one pass, two state sets) or "
+                        "dp_reduce_scatter_micro per micro-step + dp_step_update (the ZeRO-2 form)")
     return p.parse_args()
 
 
@@ -101,7 +102,18 @@ def step_bytes(wl):
 
 
 KERNEL_SOURCES = {"reduce": ("dp_kernels.cu", "dp_device.cuh"), "update": ("dp_kernels.cu", "dp_device.cuh"),
-                  "single_pass": ("dp_kernels.cu", "dp_device.cuh"), "reduce_tree": ("dp_tree.cu", "dp_device.cuh")}
+                  "single_pass": ("dp_kernels.cu", "dp_device.cuh"), "reduce_tree": ("dp_tree.cu", "dp_device.cuh"),
+                  "rs_micro": ("dp_micro.cu", "dp_device.cuh")}
+
+
+def micro_bytes(wl, comp: bool) -> int:
+    """Algorithmic bytes per parameter of the a per-micro-step launches: every gradient read once (2na), the
+    shard accumulator written at k = 0, read and written in between, read at k = a-1 (8 B an access
+    compensated, 4 plain), and gbar written once (4)."""
+    acc = 8 if comp else 4
+    if wl.a == 1:
+        return 2 * wl.n + 4
+    return 2 * wl.n * wl.a + acc + 2 * acc * (wl.a - 2) + acc + 4
 
 
 def kernel_source_hash(kernel="reduce"):
@@ -298,7 +310,10 @@ def native_main(args, wl):
     segs = synth.layout_of(wl)
     layout = dp.Layout(wl.stage, wl.n, wl.psi, segs)
     single = args.path == "single-pass"
-    bufs = StepBuffers(layout, wl.a, dev, second_set=single)
+    micro = args.path == "microstep"
+    if micro and tree:
+        raise SystemExit("--path microstep runs in ring order only")
+    bufs = StepBuffers(layout, wl.a, dev, second_set=single, micro_acc=micro)
     A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
 
     # Inputs: generated on the host into pinned buffers (kept for the end-to-end leg), then copied to HBM.
@@ -322,6 +337,8 @@ def native_main(args, wl):
     def one_step():
         if single:
             bufs.step_single_pass(A, wl.loss_scale, mode)
+        elif micro:
+            bufs.step_micro(A, wl.loss_scale, mode)
         else:
             bufs.reduce(A, wl.loss_scale, mode)
             bufs.update(A)
@@ -347,6 +364,11 @@ def native_main(args, wl):
         if single:
             bufs.step_single_pass(A, wl.loss_scale, mode)
             ev[k][1].record(stream)
+        elif micro:
+            for kk in range(wl.a):
+                bufs.reduce_micro(kk, A, wl.loss_scale, mode)
+            ev[k][1].record(stream)
+            bufs.update(A)
         else:
             bufs.reduce(A, wl.loss_scale, mode)
             ev[k][1].record(stream)
@@ -369,13 +391,16 @@ def native_main(args, wl):
     b1, b2, red_bytes, upd_bytes = step_bytes(wl)
     if single:
         red_bytes, upd_bytes = b1, 0     # one kernel streams the single-pass minimum; the repair kernel is idle
+    if micro:
+        red_bytes = micro_bytes(wl, args.sum == "compensated")
     peak, peak_kind = measured_peak()
     red_avg = sum(red_ms) / K
     upd_avg = sum(upd_ms) / K
     red_ach = red_bytes * wl.psi / (red_avg * 1e-3) / 1e9
     upd_ach = upd_bytes * wl.psi / max(1e-9, upd_avg * 1e-3) / 1e9
-    step_gbs = (b1 if single else b2) * wl.psi / (ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name, "single_pass" if single else ("reduce_tree" if tree else "reduce"))
+    step_gbs = (b1 if single else (red_bytes + upd_bytes) if micro else b2) * wl.psi / (ms * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name, "single_pass" if single else "rs_micro" if micro else
+                               ("reduce_tree" if tree else "reduce"))
 
     # End to end through the public call with host buffers: the step's gradients copied from pinned host
     # memory, the step, and the step's status read back, every step.
@@ -393,6 +418,8 @@ def native_main(args, wl):
                 bufs.grads[q].view(torch.int16).copy_(h, non_blocking=True)
             if single:
                 bufs.step_single_pass(A, wl.loss_scale, mode)
+            elif micro:
+                bufs.step_micro(A, wl.loss_scale, mode)
             else:
                 bufs.step(A, wl.loss_scale, mode)
             host_state.copy_(bufs.state, non_blocking=True)
@@ -431,6 +458,7 @@ def native_main(args, wl):
             "hbm_peak_kind": peak_kind,
             "roofline": {"bound": "hbm",
                          "kernel": ("single-pass reduce + Adam + all-gather" if single else
+                                    "per-micro-step reduce-scatter (a launches per step, summed)" if micro else
                                     "reduce (accumulate + tree reduce + average + check)" if tree else
                                     "reduce (accumulate + ring reduce-scatter + average + check)"),
                          "achieved": red_ach, "peak": peak, "unit": "GB/s", "frac": red_ach / peak,
@@ -438,7 +466,8 @@ def native_main(args, wl):
                          "peak_kind": peak_kind},
             "kernels": ({"single_pass": {"avg_ms": red_avg, "gbs": red_ach, "bytes_per_param": red_bytes},
                          "repair": {"avg_ms": upd_avg}} if single else
-                        {"reduce": {"avg_ms": red_avg, "gbs": red_ach, "bytes_per_param": red_bytes},
+                        {("rs_micro" if micro else "reduce"): {"avg_ms": red_avg, "gbs": red_ach,
+                                                                "bytes_per_param": red_bytes},
                          "update": {"avg_ms": upd_avg, "gbs": upd_ach, "bytes_per_param": upd_bytes}}),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "status": {"skipped_last_step": skipped, "error": err}, "setup_s": t_gen,

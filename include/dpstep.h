@@ -253,6 +253,35 @@ dp_status_t dp_accumulate(float* const* acc, const uint16_t* const* g, int64_t p
 dp_status_t dp_reduce_scatter_avg(float* const* gbar_shard, const float* const* acc, const dp_layout_t* layout,
                                   float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream);
 
+/* Per-micro-step reduce-scatter: the memory-saving ZeRO-2 form, in which each
+ * micro-step's gradients are reduce-scattered as soon as they exist and summed
+ * into the owner's shard accumulator, so no full-length per-rank gradient
+ * accumulator exists ("Distributed Training: Split along the Four Axes",
+ * ZeRO/FSDP paragraph: stage 2 also shards gradients; "Data vs Tensor vs
+ * Pipeline Parallelism", sharded data parallelism).  Call it for k = 0..a-1,
+ * in order, on one stream; then dp_step_update with the same gbar_shard / ws.
+ * For an element of segment owner s:
+ *   p_k = g_{s+1,k} + g_{s+2,k} + ... + g_{s,k}   (ring order, one micro-step)
+ *   A   = ((p_0 + p_1) + ...) + p_{a-1}           (in the owner's accumulator)
+ *   gbar_shard[s][local] = fl32(A * fl32(1 / (n S)))   (written by the k = a-1 call)
+ * Compensated mode carries TwoSum error terms in both sums ((H, e) =
+ * TwoSum(A_H, p_H), A_L = (A_L + e) + p_L) and ends with A_H + A_L.  This
+ * order differs from dp_step's (micro-steps summed within a rank first), so
+ * results agree with it to rounding, not bit for bit.  The k = a-1 call also
+ * counts non-finite gbar values and, like dp_step_reduce, publishes found_inf
+ * and advances t and the beta powers unless found.
+ * g: n device pointers, micro-step k of every rank, each psi bf16.
+ * acc_shard: n device shards of dp_acc_elems(dp_shard_len(layout, s),
+ *   sum_mode) floats (hi, or interleaved (hi, lo) pairs when compensated) at
+ *   local index; the caller's memory, overwritten at k = 0; unused (may be
+ *   NULL) when a = 1.
+ * gbar_shard / ws: as for dp_step_reduce; used by the k = a-1 call only.
+ * Ring order only (DP_ORDER_TREE is DP_ERR_INVALID_ARG). */
+dp_status_t dp_reduce_scatter_micro(float* const* acc_shard, float* const* gbar_shard, void* ws,
+                                    const uint16_t* const* g, int32_t k, int32_t a, const dp_layout_t* layout,
+                                    dp_adam_t adam, float loss_scale, int32_t sum_mode, dp_step_state_t* d_state,
+                                    dp_stream_t stream);
+
 /* Staged partitioned Adam.  Unless state.found_inf: t += 1, beta powers
  * advance, then for every element of every shard (stage 0: of every rank's
  * full arrays, with the owner's gbar):

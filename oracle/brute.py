@@ -96,3 +96,36 @@ def tree_gbar(grads: Sequence[np.ndarray], n: int, a: int, segs, psi: int, loss_
     p = (tot[0] + tot[1]).astype(np.float32) if arith == "f32pair" else np.asarray(tot, dtype=np.float32)
     inv = np.float32(1.0 / (float(n) * float(np.float32(loss_scale))))
     return (p * inv).astype(np.float32)
+
+
+def micro_rs_gbar(grads: Sequence[np.ndarray], n: int, a: int, segs, psi: int, loss_scale: float,
+                  arith: str = "f32") -> np.ndarray:
+    """gbar as the per-micro-step reduce-scatter (the ZeRO-2 form) computes it: each micro-step's n gradients go
+    round the simulated ring on their own (ring.py: the chunk of owner s starts at s+1), and every owner adds
+    the arriving micro-step sum to its shard accumulator, A = ((p_0 + p_1) + ...) + p_{a-1}; float32 or float32
+    (hi, lo) pairs ("f32pair": the accumulator adds (H, e) = TwoSum(A_H, p_H), A_L = (A_L + e) + p_L); then
+    hi + lo and one multiply by fl32(1 / (n S))."""
+    ring = Ring(n, segs, psi)
+    acc = {}
+    for k in range(a):
+        xs = [bf16_bits_to_f32(grads[r * a + k]) for r in range(n)]
+        loc = [(x, np.zeros_like(x)) for x in xs] if arith == "f32pair" else xs
+        red = ring.reduce_scatter(loc, arith=arith, wire_bytes=4, phase="rs%d" % k)
+        for s in range(n):
+            p = red[s]
+            if k == 0:
+                acc[s] = p
+            elif arith == "f32pair":
+                H, e = two_sum32(acc[s][0], p[0])
+                L = (acc[s][1] + e).astype(np.float32)
+                L = (L + p[1]).astype(np.float32)
+                acc[s] = (H, L)
+            else:
+                acc[s] = (acc[s] + p).astype(np.float32)
+    inv = np.float32(1.0 / (float(n) * float(np.float32(loss_scale))))
+    out = np.zeros(psi, dtype=np.float32)
+    for s in range(n):
+        v = acc[s]
+        q = (v[0] + v[1]).astype(np.float32) if arith == "f32pair" else np.asarray(v, dtype=np.float32)
+        ring._put(out, s, (q * inv).astype(np.float32))
+    return out

@@ -91,6 +91,8 @@ def _load() -> ctypes.CDLL:
                                         c_vp, c_vp]),
         "dp_step_static": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32,
                                    c_vp, c_vp]),
+        "dp_reduce_scatter_micro": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, P(dp_layout_t), dp_adam_t, c_f32,
+                                            c_i32, c_vp, c_vp]),
         "dp_checkpoint_save": (c_i32, [ctypes.c_char_p, ctypes.c_char_p, P(dp_layout_t), c_vp, c_vp, c_vp, c_vp, c_vp,
                                        c_u64, c_i32, c_vp]),
         "dp_checkpoint_load": (c_i32, [ctypes.c_char_p, ctypes.c_char_p, P(dp_layout_t), c_vp, c_vp, c_vp, c_vp, c_vp,
@@ -270,6 +272,20 @@ def dp_step_reduce(gbar_shard, ws, grads, a: int, layout: Layout, adam_: dp_adam
     gb, w = _gbar_args(layout, gbar_shard, ws)
     _check(LIB.dp_step_reduce(gb, w, _ptr_array(grads), a, ctypes.byref(layout.c), adam_, loss_scale, sum_mode,
                               _ptr(state), _stream(stream)), "dp_step_reduce")
+
+
+def dp_reduce_scatter_micro(acc_shard, gbar_shard, ws, g, k: int, a: int, layout: Layout, adam_: dp_adam_t,
+                            loss_scale: float, sum_mode: int, state, stream=None) -> None:
+    """Micro-step k of a: its n gradients (one per rank) reduce-scattered into the owner shard accumulators;
+    the last micro-step writes gbar and publishes the skip decision."""
+    _check_tensors(g, 2, [layout.psi] * len(g), "g")
+    if a > 1:
+        per = 2 if (sum_mode & 0xF) == DP_SUM_COMPENSATED else 1
+        _check_tensors(acc_shard, 4, [per * L for L in layout.shard_lens()], "acc_shard")
+    gb, w = _gbar_args(layout, gbar_shard, ws) if k == a - 1 else (None, None)
+    _check(LIB.dp_reduce_scatter_micro(_ptr_array(acc_shard) if a > 1 else None, gb, w, _ptr_array(g), k, a,
+                                       ctypes.byref(layout.c), adam_, loss_scale, sum_mode, _ptr(state),
+                                       _stream(stream)), "dp_reduce_scatter_micro")
 
 
 def dp_step_update(replicas, master, m, v, gbar_shard, ws, layout: Layout, adam_: dp_adam_t, state,

@@ -16,7 +16,8 @@ from ._lib import DP_SUM_COMPENSATED, Layout
 
 
 class StepBuffers:
-    def __init__(self, layout: Layout, a: int, device=None, with_grads: bool = True, second_set: bool = False):
+    def __init__(self, layout: Layout, a: int, device=None, with_grads: bool = True, second_set: bool = False,
+                 micro_acc: bool = False):
         self.layout = layout
         self.n, self.a, self.psi = layout.n, int(a), layout.psi
         self.device = torch.device(device or "cuda")
@@ -36,6 +37,20 @@ class StepBuffers:
         self.master1 = [torch.empty(L, dtype=torch.float32, device=dev) for L in lens] if second_set else []
         self.m1 = [torch.zeros(L, dtype=torch.float32, device=dev) for L in lens] if second_set else []
         self.v1 = [torch.zeros(L, dtype=torch.float32, device=dev) for L in lens] if second_set else []
+        # Per-micro-step reduce-scatter: the owner shard accumulators, (hi, lo) pairs (enough for either mode).
+        self.acc = [torch.empty(2 * L, dtype=torch.float32, device=dev) for L in shard] if micro_acc else []
+
+    def step_micro(self, adam_: _lib.dp_adam_t, loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED,
+                   stream=None) -> None:
+        """The step with a per-micro-step reduce-scatter (one call per micro-step), then the update."""
+        for k in range(self.a):
+            self.reduce_micro(k, adam_, loss_scale, sum_mode, stream)
+        self.update(adam_, stream=stream)
+
+    def reduce_micro(self, k: int, adam_: _lib.dp_adam_t, loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED,
+                     stream=None) -> None:
+        _lib.dp_reduce_scatter_micro(self.acc, self.gbar, None, [self.grad(r, k) for r in range(self.n)], k, self.a,
+                                     self.layout, adam_, loss_scale, sum_mode, self.state, stream=stream)
 
     def step_single_pass(self, adam_: _lib.dp_adam_t, loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED,
                          stream=None) -> None:

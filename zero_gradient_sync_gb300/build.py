@@ -10,7 +10,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdpstep.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["dp_api.cu", "dp_kernels.cu", "dp_static.cu", "dp_checkpoint.cu", "dp_tree.cu"]
+SOURCES = ["dp_api.cu", "dp_kernels.cu", "dp_static.cu", "dp_checkpoint.cu", "dp_tree.cu", "dp_micro.cu"]
 HEADERS = ["dp_device.cuh", "dp_internal.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")

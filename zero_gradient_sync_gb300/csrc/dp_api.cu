@@ -443,6 +443,32 @@ dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* c
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "reduce launch");
 }
 
+dp_status_t dp_reduce_scatter_micro(float* const* acc_shard, float* const* gbar_shard, void* ws,
+                                    const uint16_t* const* g, int32_t k, int32_t a, const dp_layout_t* layout,
+                                    dp_adam_t adam, float loss_scale, int32_t sum_mode, dp_step_state_t* d_state,
+                                    dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  if (a < 1 || k < 0 || k >= a) return fail(DP_ERR_INVALID_ARG, "micro-step k = %d of a = %d", k, a);
+  StepScalars s;
+  if ((st = scalars(P, &adam, loss_scale, sum_mode, s)) != DP_OK) return st;
+  if (s.order != DP_ORDER_RING) return fail(DP_ERR_INVALID_ARG, "dp_reduce_scatter_micro: ring order only");
+  if ((st = check_full_arrays(P, (const void* const*)g, P.n, "g")) != DP_OK) return st;
+  if (a > 1) {
+    int64_t lens[DP_MAX_N];
+    for (int r = 0; r < P.n; ++r) lens[r] = P.shard_len[r] * (s.mode == DP_SUM_COMPENSATED ? 2 : 1);
+    if ((st = check_ptr_array((const void* const*)acc_shard, P.n, "acc_shard", lens)) != DP_OK) return st;
+  }
+  float* gb[DP_MAX_N] = {nullptr};
+  if (k == a - 1 && (st = gbar_ptrs(P, gbar_shard, ws, gb)) != DP_OK) return st;
+  if ((st = check_state(d_state)) != DP_OK) return st;
+  LaunchCount lc;
+  cudaError_t e = dp::launch_rs_micro(P, g, a > 1 ? acc_shard : nullptr, gb, k, a, s, d_state, (cudaStream_t)stream,
+                                      &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "reduce_scatter_micro launch");
+}
+
 dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
                            const float* const* gbar_shard, void* ws, const dp_layout_t* layout, dp_adam_t adam,
                            const dp_step_state_t* d_state, dp_stream_t stream) {

@@ -43,6 +43,10 @@ cudaError_t launch_reduce_tree(const Plan& P, const uint16_t* const* g, int a, f
                                uint64_t* launches);
 cudaError_t launch_rs_tree(const Plan& P, const float* const* acc, float* const* gbar, const StepScalars& s,
                            dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+// Per-micro-step reduce-scatter (dp_micro.cu): micro-step k of a into the owner shard accumulators.
+cudaError_t launch_rs_micro(const Plan& P, const uint16_t* const* g, float* const* acc, float* const* gbar, int k,
+                            int a, const StepScalars& s, dp_step_state_t* st, cudaStream_t stream,
+                            uint64_t* launches);
 cudaError_t launch_single_pass(const Plan& P, const uint16_t* const* g, int a, uint16_t* const* rep,
                                float* const* master2, float* const* m2, float* const* v2, const StepScalars& s,
                                dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
