@@ -120,11 +120,23 @@ def assert_close_f32(x: np.ndarray, ref: np.ndarray, name: str, scale: float = 1
         name, bad.size, bad[:5], x[bad[:5]], ref[bad[:5]])
 
 
+def bf16_value(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def assert_replicas(reps: List[np.ndarray], ref: List[np.ndarray], ulps: int = 1) -> None:
+    """Within 1 bf16 ulp -- or, where the master's absolute tolerance term dominates (|theta| below ~5e-4), within
+    that tolerance plus one bf16 ulp: a replica is bf16_rne of the master, so it can differ by no more than the
+    master it rounds."""
     for r, (x, y) in enumerate(zip(reps, ref)):
         d = np.abs(bf16_ord(x) - bf16_ord(y))
-        bad = np.nonzero(d > ulps)[0]
-        assert bad.size == 0, "replica %d: %d elements beyond %d bf16 ulp, first %s" % (r, bad.size, ulps, bad[:5])
+        far = np.nonzero(d > ulps)[0]
+        if far.size:
+            xv, yv = bf16_value(x[far]), bf16_value(y[far])
+            ulp = np.abs(bf16_value(y[far] ^ 1) - yv)
+            ok = np.abs(xv - yv) <= ABS + REL * np.abs(yv) + ulp
+            far = far[~ok]
+        assert far.size == 0, "replica %d: %d elements beyond %d bf16 ulp, first %s" % (r, far.size, ulps, far[:5])
     for x in reps[1:]:
         assert np.array_equal(x, reps[0]), "replicas differ from each other"
 
