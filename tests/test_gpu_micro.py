@@ -104,7 +104,7 @@ def test_micro_skip_and_determinism(dev):
     # -inf in a middle micro-step of one rank: the whole step is skipped
     b2 = upload_micro(c)
     before = gu.snapshot(b2)
-    b2.grad(3, 1)[12345:12346].view(torch.int16).fill_(synth.BF16_NEG_INF)
+    b2.grad(3, 1)[12345:12346].view(torch.int16).fill_(synth.BF16_NEG_INF - 0x10000)   # as a signed 16-bit word
     b2.step_micro(A, wl.loss_scale, COMP)
     st = dp.read_state(b2.state)
     assert (st["found_inf"], st["nonfinite"], st["t"]) == (1, 1, 0)
