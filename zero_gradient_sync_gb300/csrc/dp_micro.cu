@@ -13,6 +13,10 @@
 // ranks in batches of four so 4 loads are in flight besides the accumulator's) and reading / writing the
 // accumulator at the owner's local index.  The last micro-step's launch writes gbar instead, counts
 // non-finite values and publishes the skip decision and t like pass A of the step.
+//
+// With one micro-step (a = 1) the per-micro-step order is the step's own ring order, operation for
+// operation, so the same kernel also serves as pass A of dp_step for a = 1: with few inputs per tile it
+// streams faster than the bulk-copy pipeline, whose per-stage overhead is then spread over too little work.
 #include "dp_device.cuh"
 #include "dp_internal.h"
 
@@ -34,6 +38,7 @@ struct MicroParams {
   double beta1, beta2;
   float inv;
   int32_t n;
+  ScalerK scaler;   // enabled (last launch only): unscale by the device-resident scale, then update it
   SegTable<MAXSEG> seg;
 };
 
@@ -50,13 +55,32 @@ template <int MAXSEG, bool COMP, int FLAGS>
 __global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_constant__ MicroParams<MAXSEG> p) {
   constexpr bool FIRST = (FLAGS & RM_FIRST) != 0, LAST = (FLAGS & RM_LAST) != 0;
   __shared__ unsigned long long s_count;
-  if (LAST && threadIdx.x == 0) s_count = 0ull;
+  __shared__ float s_inv;
+  __shared__ int s_bad_scale;
+  if (LAST && threadIdx.x == 0) {
+    s_count = 0ull;
+    float inv = p.inv;
+    int bad_scale = 0;
+    if (p.scaler.enabled) {
+      // fl32(1 / (n S)) from the device-resident scale, as the host computes it for a fixed scale.
+      const float sc = *reinterpret_cast<volatile const float*>(&p.state->loss_scale);
+      inv = (float)(1.0 / ((double)p.n * (double)sc));
+      if (!(sc > 0.0f) || nonfinite(sc) || !(inv >= 1.17549435e-38f) || nonfinite(inv)) {
+        record_error(p.state, DP_ERR_INVALID_ARG);
+        bad_scale = 1;    // skip the work; the finish sees the error and skips the step
+        inv = 0.0f;
+      }
+    }
+    s_inv = inv;
+    s_bad_scale = bad_scale;
+  }
   if (LAST) __syncthreads();
+  const float inv = LAST ? s_inv : 0.0f;
   const int n = p.n;
   const int64_t psi = p.seg.psi;
   unsigned bad = 0;
   TileWalker<MAXSEG> walk;
-  for (int tile = blockIdx.x; tile < p.seg.ntiles; tile += gridDim.x) {
+  for (int tile = (LAST && s_bad_scale) ? p.seg.ntiles : blockIdx.x; tile < p.seg.ntiles; tile += gridDim.x) {
     const Tile t = walk.at(p.seg, tile);
     const int64_t A = t.start & ~int64_t(7), B = (t.end + 7) & ~int64_t(7);
     const int64_t delta = t.loff - t.goff;
@@ -176,7 +200,7 @@ __global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_const
       } else {
         float o[RM_EPT];
 #pragma unroll
-        for (int u = 0; u < RM_EPT; ++u) o[u] = __fmul_rn(COMP ? __fadd_rn(hv[u], lv[u]) : hv[u], p.inv);
+        for (int u = 0; u < RM_EPT; ++u) o[u] = __fmul_rn(COMP ? __fadd_rn(hv[u], lv[u]) : hv[u], inv);
         float* dst = p.gbar[t.owner] + j;
         if (whole && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
           *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
@@ -200,7 +224,8 @@ __global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_const
     for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
     if ((threadIdx.x & 31) == 0 && c) atomicAdd(&s_count, c);
     __syncthreads();
-    if (threadIdx.x == 0) finish_reduction(p.state, s_count, s_count != 0ull, 1, p.beta1, p.beta2);
+    if (threadIdx.x == 0)
+      finish_reduction(p.state, s_count, (s_count != 0ull) || s_bad_scale, 1, p.beta1, p.beta2, &p.scaler, 0);
   }
 }
 
@@ -244,6 +269,7 @@ cudaError_t launch_micro_t(const Plan& P, const uint16_t* const* g, float* const
   prm.beta2 = (double)s.beta2;
   prm.inv = s.inv;
   prm.n = P.n;
+  prm.scaler = s.scaler;
   fill_micro_table(prm.seg, P);
   auto kern = rs_micro_kernel<MAXSEG, COMP, FLAGS>;
   kern<<<micro_grid(kern, P.ntiles), RM_THREADS, 0, stream>>>(prm);
