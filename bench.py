@@ -101,9 +101,11 @@ def step_bytes(wl):
     return b1, b1 + 8, 2 * wl.n * wl.a + 4, 4 + 24 + 2 * wl.n
 
 
-KERNEL_SOURCES = {"reduce": ("dp_kernels.cu", "dp_device.cuh"), "update": ("dp_kernels.cu", "dp_device.cuh"),
-                  "single_pass": ("dp_kernels.cu", "dp_device.cuh"), "reduce_tree": ("dp_tree.cu", "dp_device.cuh"),
-                  "rs_micro": ("dp_micro.cu", "dp_device.cuh")}
+KERNEL_SOURCES = {"reduce": ("dp_kernels.cu", "dp_device.cuh", "dp_launch.h"),
+                  "update": ("dp_kernels.cu", "dp_device.cuh", "dp_launch.h"),
+                  "single_pass": ("dp_kernels.cu", "dp_device.cuh", "dp_launch.h"),
+                  "reduce_tree": ("dp_tree.cu", "dp_device.cuh", "dp_launch.h"),
+                  "rs_micro": ("dp_micro.cu", "dp_device.cuh", "dp_launch.h")}
 
 
 def micro_bytes(wl, comp: bool) -> int:

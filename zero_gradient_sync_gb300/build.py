@@ -11,7 +11,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdpstep.so")
 BUILD = os.path.join(HERE, "_build")
 SOURCES = ["dp_api.cu", "dp_kernels.cu", "dp_static.cu", "dp_checkpoint.cu", "dp_tree.cu", "dp_micro.cu"]
-HEADERS = ["dp_device.cuh", "dp_internal.h"]
+HEADERS = ["dp_device.cuh", "dp_internal.h", "dp_launch.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -18,6 +18,7 @@
 
 #include "dp_device.cuh"
 #include "dp_internal.h"
+#include "dp_launch.h"
 
 namespace dp {
 
@@ -782,40 +783,8 @@ __global__ void selftest_wait_kernel(dp_step_state_t* st, uint64_t timeout_ns) {
 
 // ============================================================================ launchers
 
-static int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int v = 0;
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = v > 0 ? v : 148;
-  }
-  return cached[dev];
-}
 
-template <int MAXSEG>
-static void fill_seg(SegTable<MAXSEG>& T, const Plan& P) {
-  T.psi = P.psi;
-  T.nseg = P.nseg;
-  T.ntiles = P.ntiles;
-  for (int k = 0; k <= P.nseg; ++k) {
-    T.e[k].goff = P.e[k].goff;
-    T.e[k].loff = P.e[k].loff;
-    T.e[k].tile0 = P.e[k].tile0;
-    T.e[k].owner = P.e[k].owner;
-  }
-}
 
-template <typename K>
-static int occupancy_grid(K kernel, int threads, size_t smem, int ntiles) {
-  int per_sm = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
-  if (per_sm < 1) per_sm = 1;
-  long long g = (long long)sm_count() * per_sm;
-  if (ntiles < g) g = ntiles;
-  return (int)(g < 1 ? 1 : g);
-}
 
 // Single-pass inputs beyond the reduction's: optimizer-state sets and replicas.
 struct FusedArgs {

@@ -19,6 +19,7 @@
 // streams faster than the bulk-copy pipeline, whose per-stage overhead is then spread over too little work.
 #include "dp_device.cuh"
 #include "dp_internal.h"
+#include "dp_launch.h"
 
 namespace dp {
 namespace {
@@ -229,32 +230,6 @@ __global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_const
   }
 }
 
-template <int MAXSEG>
-void fill_micro_table(SegTable<MAXSEG>& T, const Plan& P) {
-  T.psi = P.psi;
-  T.nseg = P.nseg;
-  T.ntiles = P.ntiles;
-  for (int k = 0; k <= P.nseg; ++k) {
-    T.e[k].goff = P.e[k].goff;
-    T.e[k].loff = P.e[k].loff;
-    T.e[k].tile0 = P.e[k].tile0;
-    T.e[k].owner = P.e[k].owner;
-  }
-}
-
-template <typename K>
-int micro_grid(K kernel, int ntiles) {
-  int dev = 0, sms = 0, per_sm = 1;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                   cudaSuccess || sms < 1)
-    sms = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, RM_THREADS, 0) != cudaSuccess || per_sm < 1)
-    per_sm = 1;
-  long long g = (long long)sms * per_sm;
-  if (ntiles < g) g = ntiles;
-  return (int)(g < 1 ? 1 : g);
-}
-
 template <int MAXSEG, bool COMP, int FLAGS>
 cudaError_t launch_micro_t(const Plan& P, const uint16_t* const* g, float* const* acc, float* const* gbar,
                            const StepScalars& s, dp_step_state_t* st, cudaStream_t stream) {
@@ -270,9 +245,9 @@ cudaError_t launch_micro_t(const Plan& P, const uint16_t* const* g, float* const
   prm.inv = s.inv;
   prm.n = P.n;
   prm.scaler = s.scaler;
-  fill_micro_table(prm.seg, P);
+  fill_seg(prm.seg, P);
   auto kern = rs_micro_kernel<MAXSEG, COMP, FLAGS>;
-  kern<<<micro_grid(kern, P.ntiles), RM_THREADS, 0, stream>>>(prm);
+  kern<<<occupancy_grid(kern, RM_THREADS, 0, P.ntiles), RM_THREADS, 0, stream>>>(prm);
   return cudaGetLastError();
 }
 

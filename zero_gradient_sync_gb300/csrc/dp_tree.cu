@@ -16,6 +16,7 @@
 // rs_tree_kernel: the same tree over the staged per-rank accumulators, one element per thread.
 #include "dp_device.cuh"
 #include "dp_internal.h"
+#include "dp_launch.h"
 
 namespace dp {
 namespace {
@@ -381,33 +382,6 @@ __global__ void __launch_bounds__(256) rs_tree_kernel(const __grid_constant__ Rs
 
 // ---------------------------------------------------------------- launchers
 
-template <int MAXSEG>
-void fill_table(SegTable<MAXSEG>& T, const Plan& P) {
-  T.psi = P.psi;
-  T.nseg = P.nseg;
-  T.ntiles = P.ntiles;
-  for (int k = 0; k <= P.nseg; ++k) {
-    T.e[k].goff = P.e[k].goff;
-    T.e[k].loff = P.e[k].loff;
-    T.e[k].tile0 = P.e[k].tile0;
-    T.e[k].owner = P.e[k].owner;
-  }
-}
-
-// Resident CTAs of `kernel` on every SM, capped by the tile count (at least 1: every CTA joins the finish).
-template <typename K>
-int resident_grid(K kernel, int threads, size_t smem, int ntiles) {
-  int dev = 0, sms = 0, per_sm = 1;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                   cudaSuccess || sms < 1)
-    sms = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
-    per_sm = 1;
-  long long g = (long long)sms * per_sm;
-  if (ntiles < g) g = ntiles;
-  return (int)(g < 1 ? 1 : g);
-}
-
 template <int MAXSEG, bool COMP, int LEVELS>
 cudaError_t launch_tree_t(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
                           const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream) {
@@ -423,7 +397,7 @@ cudaError_t launch_tree_t(const Plan& P, const uint16_t* const* g, int a, float*
   prm.a = a;
   prm.advance = advance;
   prm.scaler = s.scaler;
-  fill_table(prm.seg, P);
+  fill_seg(prm.seg, P);
   auto kern = reduce_tree_kernel<MAXSEG, COMP, LEVELS>;
   // The opt-in shared-memory size is set once per device (not inside a stream capture on later calls).
   static bool attr_set[64] = {false};
@@ -436,7 +410,7 @@ cudaError_t launch_tree_t(const Plan& P, const uint16_t* const* g, int a, float*
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   // One CTA per SM (every CTA joins the grid-wide finish, so at least one runs even with no tiles).
-  kern<<<resident_grid(kern, TT_THREADS, TT_SMEM, P.ntiles), TT_THREADS, TT_SMEM, stream>>>(prm);
+  kern<<<occupancy_grid(kern, TT_THREADS, TT_SMEM, P.ntiles), TT_THREADS, TT_SMEM, stream>>>(prm);
   return cudaGetLastError();
 }
 
@@ -458,9 +432,9 @@ cudaError_t launch_rs_tree_t(const Plan& P, const float* const* acc, float* cons
   prm.state = st;
   prm.inv = s.inv;
   prm.n = P.n;
-  fill_table(prm.seg, P);
+  fill_seg(prm.seg, P);
   auto kern = rs_tree_kernel<MAXSEG, COMP>;
-  kern<<<resident_grid(kern, 256, 0, P.ntiles), 256, 0, stream>>>(prm);
+  kern<<<occupancy_grid(kern, 256, 0, P.ntiles), 256, 0, stream>>>(prm);
   return cudaGetLastError();
 }
 
