@@ -7,7 +7,9 @@
   it hop by hop (ring.py), after each rank has accumulated its micro-steps
   locally with no communication ("Distributed Training: Split along the Four
   Axes", worked example: accumulate locally, one all-reduce after the a-th
-  micro-step), in float32 or float32 (hi, lo) pairs.  This is the reduction
+  micro-step), in float32 or float32 (hi, lo) pairs; or ("f32chain") with
+  every rank folding its micro-steps one at a time into the (hi, lo) pair that
+  arrives from its left neighbour.  This is the reduction
   order the GPU path promises, derived from message passing rather than from
   the GPU code.
 * tree_gbar: the same local accumulation, then the ranks' sums added up the
@@ -68,15 +70,19 @@ def local_accumulate(grads: Sequence[np.ndarray], n: int, a: int, arith: str) ->
 
 def ring_gbar(grads: Sequence[np.ndarray], n: int, a: int, segs, psi: int, loss_scale: float,
               arith: str = "f32") -> np.ndarray:
-    """gbar as the ring computes it: float32 partials ("f32") or float32 (hi, lo) pairs ("f32pair"),
-    then hi + lo, then one multiply by fl32(1 / (n S))."""
-    loc = local_accumulate(grads, n, a, arith)
+    """gbar as the ring computes it: float32 partials ("f32") or float32 (hi, lo) pairs ("f32pair") after
+    rank-local accumulation, or a float32 (hi, lo) pair into which every rank folds its unsummed micro-steps
+    ("f32chain"); then hi + lo, then one multiply by fl32(1 / (n S))."""
+    if arith == "f32chain":
+        loc = [[bf16_bits_to_f32(grads[r * a + k]) for k in range(a)] for r in range(n)]
+    else:
+        loc = local_accumulate(grads, n, a, arith)
     ring = Ring(n, segs, psi)
     red = ring.reduce_scatter(loc, arith=arith, wire_bytes=4)
     inv = np.float32(1.0 / (float(n) * float(np.float32(loss_scale))))
     out = np.zeros(psi, dtype=np.float32)
     for s in range(n):
-        if arith == "f32pair":
+        if arith in ("f32pair", "f32chain"):
             H, L = red[s]
             p = (H + L).astype(np.float32)
         else:

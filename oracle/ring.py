@@ -24,7 +24,11 @@ n-1 hops as ((g_{s+1} + g_{s+2}) + ...) + g_s.
 Arithmetic of a hop, selectable: "f64" (float64 adds), "f32" (float32 adds)
 or "f32pair" (the partial travels as a float32 (hi, lo) pair; the receiver
 adds its own (hi, lo) with Knuth's TwoSum error-free transformation, TAOCP
-vol. 2 section 4.2.2, and accumulates the error terms in lo).
+vol. 2 section 4.2.2, and accumulates the error terms in lo).  "f32chain":
+the partial travels as a float32 (hi, lo) pair too, but a rank's contribution
+is its list of micro-step gradients, not yet summed, and the receiver folds
+them into the pair one at a time (hi, e) = TwoSum(hi, x), lo = lo + e; the
+first rank of a chunk starts the pair at (its first micro-step, 0).
 """
 from __future__ import annotations
 
@@ -101,11 +105,28 @@ class Ring:
         tr = self.traffic.setdefault(phase, Traffic(n))
 
         def own(r: int, s: int):
+            if arith == "f32chain":
+                return [self._take(x, s) for x in local[r]]
             if arith == "f32pair":
                 return (self._take(local[r][0], s), self._take(local[r][1], s))
             return self._take(local[r], s)
 
+        def fold(pair, xs):
+            H, L = pair
+            for x in xs:
+                H, e = two_sum32(H, x)
+                L = (L + e).astype(np.float32)
+            return (H, L)
+
+        def start(mine):
+            if arith != "f32chain":
+                return mine
+            first = mine[0].astype(np.float32)
+            return fold((first, np.zeros_like(first)), mine[1:])
+
         def combine(recv, mine):
+            if arith == "f32chain":
+                return fold(recv, mine)
             if arith == "f64":
                 return recv.astype(np.float64) + mine.astype(np.float64)
             if arith == "f32":
@@ -116,13 +137,13 @@ class Ring:
             return (H, L)
 
         if n == 1:
-            return {0: own(0, 0)}
+            return {0: start(own(0, 0))}
         inbox: List = [None] * n
         for t in range(n - 1):
             out = []
             for r in range(n):
                 s = (r - 1 - t) % n
-                payload = own(r, s) if t == 0 else inbox[r][1]
+                payload = start(own(r, s)) if t == 0 else inbox[r][1]
                 if t > 0 and inbox[r][0] != s:
                     raise RuntimeError("ring schedule broken")
                 elems = self.chunk_len(s)
