@@ -421,12 +421,11 @@ static dp_status_t prepare_reduce(const Plan& P, const uint16_t* const* grads, i
   return st;
 }
 
-// Pass A in the order s names.  With one micro-step the ring order is that of the per-micro-step kernel
-// (p = g_{s+1} + ... + g_s, then gbar), which streams few inputs per tile faster than the pipeline kernel.
+// Pass A in the order s names.  (With one micro-step the ring kernel and the per-micro-step kernel perform
+// the same operations, p = g_{s+1} + ... + g_s then gbar; the ring kernel streams faster.)
 static cudaError_t launch_pass_a(const Plan& P, const uint16_t* const* grads, int a, float* const* gb,
                                  const StepScalars& s, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
   if (s.order == DP_ORDER_TREE) return dp::launch_reduce_tree(P, grads, a, gb, s, 1, st, stream, launches);
-  if (a == 1) return dp::launch_rs_micro(P, grads, nullptr, gb, 0, 1, s, st, stream, launches);
   return dp::launch_reduce(P, grads, a, gb, s, 1, st, stream, launches);
 }
 

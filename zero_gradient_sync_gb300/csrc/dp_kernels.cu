@@ -1,20 +1,23 @@
 // Kernels of the fused data-parallel step and their launchers (sm_103a).
 //
 // reduce (fused pass A): the n*a bf16 micro-step gradients of a tile are
-//   streamed once from HBM into a ring of shared-memory stages by one
-//   producer thread issuing 1-D bulk copies (cp.async.bulk, mbarrier
-//   transaction counts); 16 consumer warps fold each stage into per-element
-//   accumulators in the fixed order (micro-steps of a rank, then ranks in
-//   ring order s+1..s), scale by fl32(1/(n S)), count non-finite results and
-//   write gbar to the owner's shard.  The last CTA publishes the step's
-//   skip flag and advances t.
+//   streamed once from HBM into a ring of shared-memory stages (two inputs,
+//   two 15 KB bulk copies, per stage) by one producer thread issuing 1-D
+//   bulk copies (cp.async.bulk, mbarrier transaction counts); 15 consumer
+//   warps fold each stage into per-element accumulators in the fixed ring
+//   order (ranks s+1..s, each rank's micro-steps 0..a-1), scale by
+//   fl32(1/(n S)), count non-finite results and write gbar to the owner's
+//   shard.  The last CTA publishes the step's skip flag and advances t.
 // update (fused pass B): unless skipped, Adam on the fp32 master/m/v shard
 //   (16-byte vector loads/stores in local index space) and the bf16 image of
 //   the new master staged in shared memory, then bulk-stored into all n
 //   replicas (cp.async.bulk shared->global) at global index.
 // Staged kernels (accumulate, rs_avg, adam = update without replicas,
-//   allgather, advance) compute bit-identical results one phase at a time.
+//   allgather, advance) compute the same step one phase at a time: bit-
+//   identical in plain arithmetic; compensated, the staged form keeps one
+//   (hi, lo) pair per rank where pass A carries one pair through all inputs.
 #include <algorithm>
+#include <type_traits>
 
 #include "dp_device.cuh"
 #include "dp_internal.h"
@@ -28,17 +31,22 @@ constexpr int RA_CWARPS = 15;
 constexpr int RA_CTHREADS = RA_CWARPS * 32;    // consumer threads
 constexpr int RA_EPT = 16;                     // elements per consumer thread: two 16-byte shared loads
 constexpr int RA_THREADS = RA_CTHREADS + 32;   // + one producer warp: 16 warps, 4 per SM sub-partition
-constexpr int RA_STAGES = 12;
-constexpr int RA_STAGE_BYTES = TILE * 2;       // one tile of one bf16 input: a 15 KB bulk copy
+constexpr int RA_NPS = 2;                      // inputs per stage: two 15 KB bulk copies on one barrier
+constexpr int RA_IN_BYTES = TILE * 2;          // one tile of one bf16 input
+constexpr int RA_STAGE_BYTES = RA_NPS * RA_IN_BYTES;
 constexpr int RA_GBAR_FLOATS = TILE + 16;      // single pass: the tile's gbar (+16: last group's overhang)
 constexpr int RA_EXTRA_FUSED = RA_GBAR_FLOATS * 4 + TILE * 2;   // + the tile's bf16 staging
+// 180 KB of stages in flight; the single pass gives one stage up for its gbar and staging tiles.
 template <bool FUSED>
-__host__ __device__ constexpr int ra_bar_offset() { return RA_STAGES * RA_STAGE_BYTES + (FUSED ? RA_EXTRA_FUSED : 0); }
+__host__ __device__ constexpr int ra_stages() { return FUSED ? 5 : 6; }
 template <bool FUSED>
-__host__ __device__ constexpr int ra_smem() { return ra_bar_offset<FUSED>() + 2 * RA_STAGES * 8 + 32; }
+__host__ __device__ constexpr int ra_bar_offset() { return ra_stages<FUSED>() * RA_STAGE_BYTES + (FUSED ? RA_EXTRA_FUSED : 0); }
+template <bool FUSED>
+__host__ __device__ constexpr int ra_smem() { return ra_bar_offset<FUSED>() + 2 * ra_stages<FUSED>() * 8 + 32; }
 static_assert(ra_smem<true>() + 64 <= 227 * 1024, "single-pass shared memory fits one CTA");
+static_assert(ra_smem<false>() + 64 <= 227 * 1024, "shared memory fits one CTA");
 static_assert(TILE == RA_CTHREADS * RA_EPT, "one 16-element group per consumer thread");
-static_assert(RA_STAGE_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
+static_assert(RA_IN_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
 
 template <int MAXSEG>
 struct ReduceParams {
@@ -60,11 +68,12 @@ struct ReduceParams {
 };
 
 // Ring-buffer position of a stage: slot and the parity of its current use.
+template <int NSTAGES>
 struct RingPos {
   uint32_t slot = 0, phase = 0, count = 0;
   __device__ __forceinline__ void next() {
     ++count;
-    if (++slot == RA_STAGES) {
+    if (++slot == NSTAGES) {
       slot = 0;
       phase ^= 1u;
     }
@@ -153,16 +162,43 @@ __device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, cons
   }
 }
 
+// Fold input HH of a stage (8 words = 16 bf16 of this thread) into the accumulators, ring order.
+//  compensated: one (H, L) pair through the whole sequence, (H, e) = TwoSum(H, x), L = L + e (first: H = x);
+//  plain: each rank's micro-steps summed left to right in h (kfirst starts a rank), and at the rank's last
+//  micro-step (klast) h joins the ring sum, H = ((h_{s+1} + h_{s+2}) + ...) + h_s.
+template <bool COMP, int HH>
+__device__ __forceinline__ void fold_input(f2_t (&H)[8], f2_t (&L)[8], f2_t (&h)[8], const uint32_t (&w)[8 * RA_NPS],
+                                           bool first, bool kfirst, bool klast, bool first_rank) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const f2_t x = bf16x2_to_f2(w[8 * HH + u]);
+    if (COMP) {
+      if (first) {
+        H[u] = x;
+        L[u] = 0ull;
+      } else {
+        f2_t e;
+        H[u] = f2_two_sum(H[u], x, e);
+        L[u] = f2_add(L[u], e);
+      }
+    } else {
+      h[u] = kfirst ? x : f2_add(h[u], x);
+      if (klast) H[u] = first_rank ? h[u] : f2_add(H[u], h[u]);
+    }
+  }
+}
+
 template <int MAXSEG, bool COMP, bool FUSED>
 __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceParams<MAXSEG> p) {
+  constexpr int NST = ra_stages<FUSED>();
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
-  float* s_g = reinterpret_cast<float*>(smem + RA_STAGES * RA_STAGE_BYTES);
-  uint16_t* s_stage = reinterpret_cast<uint16_t*>(smem + RA_STAGES * RA_STAGE_BYTES + RA_GBAR_FLOATS * 4);
+  float* s_g = reinterpret_cast<float*>(smem + NST * RA_STAGE_BYTES);
+  uint16_t* s_stage = reinterpret_cast<uint16_t*>(smem + NST * RA_STAGE_BYTES + RA_GBAR_FLOATS * 4);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ra_bar_offset<FUSED>());
-  uint64_t* empty = full + RA_STAGES;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + RA_STAGES);
-  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + RA_STAGES + 1);
+  uint64_t* empty = full + NST;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + NST);
+  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + NST + 1);
   __shared__ float s_inv;
   __shared__ float s_k[2];
   __shared__ int s_cur;
@@ -174,7 +210,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
   const int64_t p8 = psi & ~int64_t(7);
 
   if (tid == 0) {
-    for (int s = 0; s < RA_STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), RA_CWARPS);
     }
@@ -207,44 +243,52 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
   if (warp == RA_CWARPS) {
     // ------------------------------------------------------------ producer: one thread issues every copy
     if (lane == 0) {
-      RingPos rp;
+      RingPos<NST> rp;
       TileWalker<MAXSEG> walk;
+      const int nin = n * a;
       for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
         const Tile t = walk.at(p.seg, tile);
         const int64_t A = t.start & ~int64_t(7);
         int64_t B = (t.end + 7) & ~int64_t(7);
         if (B > p8) B = p8;
         const uint32_t bytes = B > A ? (uint32_t)(B - A) * 2u : 0u;
-        int r = t.owner + 1 == n ? 0 : t.owner + 1;
-        for (int j = 0; j < n && !*s_abort; ++j) {
-          for (int k = 0; k < a; ++k) {
-            if (rp.count >= (uint32_t)RA_STAGES &&
-                !mbar_wait_bounded(smem_u32(&empty[rp.slot]), rp.phase ^ 1u, p.timeout_ns, s_abort)) {
-              if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
-              *s_abort = 1;
-              break;
-            }
-            const uint32_t fb = smem_u32(&full[rp.slot]);
-            mbar_arrive_expect_tx(fb, bytes);
-            if (bytes) bulk_g2s(smem_u32(stages + rp.slot * RA_STAGE_BYTES), p.g[r * a + k] + A, bytes, fb);
-            rp.next();
+        // Inputs in ring order: rank owner+1 first, its micro-steps 0..a-1, then the next rank; two per stage.
+        int r = t.owner + 1 == n ? 0 : t.owner + 1, k = 0;
+        for (int q = 0; q < nin && !*s_abort; q += RA_NPS) {
+          if (rp.count >= (uint32_t)NST &&
+              !mbar_wait_bounded(smem_u32(&empty[rp.slot]), rp.phase ^ 1u, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+            *s_abort = 1;
+            break;
           }
-          if (++r == n) r = 0;
+          const int cnt = nin - q < RA_NPS ? nin - q : RA_NPS;
+          const uint32_t fb = smem_u32(&full[rp.slot]);
+          mbar_arrive_expect_tx(fb, bytes * (uint32_t)cnt);
+          for (int h = 0; h < cnt; ++h) {
+            if (bytes)
+              bulk_g2s(smem_u32(stages + rp.slot * RA_STAGE_BYTES + h * RA_IN_BYTES), p.g[r * a + k] + A, bytes, fb);
+            if (++k == a) {
+              k = 0;
+              if (++r == n) r = 0;
+            }
+          }
+          rp.next();
         }
       }
       // Never leave with copies in flight: wait for the newest issued phase of every slot.
       if (*s_abort) {
         const uint32_t it = rp.count;
-        const uint32_t first = it > (uint32_t)RA_STAGES ? it - RA_STAGES : 0u;
+        const uint32_t first = it > (uint32_t)NST ? it - NST : 0u;
         for (uint32_t x = first; x < it; ++x)
-          (void)mbar_wait_bounded(smem_u32(&full[x % RA_STAGES]), (x / RA_STAGES) & 1u, p.timeout_ns, nullptr);
+          (void)mbar_wait_bounded(smem_u32(&full[x % NST]), (x / NST) & 1u, p.timeout_ns, nullptr);
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers: 16 elements per thread
     const f2_t inv2 = f2_pack(s_inv, s_inv);
-    RingPos rp;
+    const int nin = n * a;
+    RingPos<NST> rp;
     TileWalker<MAXSEG> walk;
     bool live = true;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -255,29 +299,55 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
       const bool active = e0 < B;
       const bool tailgrp = active && (e0 + RA_EPT > p8);
 
-      // One stage: wait for its bytes, take this thread's 16 values, release the slot.  The shared abort
+      // One stage: wait for its bytes, take this thread's 16 values of each of its cnt inputs, release the slot.
+      // FULL (the tile is a whole cell, every thread active, no buffer tail): plain shared loads only.
+      // Otherwise inactive threads take zeros and the group holding the buffer's last partial 8 elements is
+      // read from global memory (r0, k0: rank and micro-step of the stage's first input).  The shared abort
       // flag is only read inside a wait that did not succeed at once; `live` is this thread's view.
-      auto take = [&](const uint16_t* src, uint32_t (&w)[8]) {
+      auto take = [&](auto full_tag, int cnt, int r0, int k0, uint32_t (&w)[8 * RA_NPS]) {
+        constexpr bool FULL = decltype(full_tag)::value;
         if (live && !mbar_wait_bounded(smem_u32(&full[rp.slot]), rp.phase, p.timeout_ns, s_abort)) {
           if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
           *s_abort = 1;
           live = false;
         }
+        const unsigned char* sp = stages + rp.slot * RA_STAGE_BYTES + 2 * RA_EPT * tid;
+        if constexpr (FULL) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) w[u] = 0u;
-        if (active && live) {
-          if (!tailgrp) {
-            const unsigned char* sp = stages + rp.slot * RA_STAGE_BYTES + 2 * RA_EPT * tid;
-            const uint4 v0 = *reinterpret_cast<const uint4*>(sp);
-            const uint4 v1 = *reinterpret_cast<const uint4*>(sp + 16);
-            w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-            w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-          } else {
-            // The group holding the buffer's last partial 8 elements is read from global memory.
+          for (int hh = 0; hh < RA_NPS; ++hh) {
+            if (hh < cnt) {
+              const uint4 v0 = *reinterpret_cast<const uint4*>(sp + hh * RA_IN_BYTES);
+              const uint4 v1 = *reinterpret_cast<const uint4*>(sp + hh * RA_IN_BYTES + 16);
+              w[8 * hh + 0] = v0.x; w[8 * hh + 1] = v0.y; w[8 * hh + 2] = v0.z; w[8 * hh + 3] = v0.w;
+              w[8 * hh + 4] = v1.x; w[8 * hh + 5] = v1.y; w[8 * hh + 6] = v1.z; w[8 * hh + 7] = v1.w;
+            }
+          }
+        } else {
 #pragma unroll
-            for (int u = 0; u < RA_EPT; ++u) {
-              const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
-              w[u >> 1] |= (u & 1) ? (b << 16) : b;
+          for (int u = 0; u < 8 * RA_NPS; ++u) w[u] = 0u;
+          if (active && live) {
+            int rr = r0, kk = k0;
+#pragma unroll
+            for (int hh = 0; hh < RA_NPS; ++hh) {
+              if (hh < cnt) {
+                if (!tailgrp) {
+                  const uint4 v0 = *reinterpret_cast<const uint4*>(sp + hh * RA_IN_BYTES);
+                  const uint4 v1 = *reinterpret_cast<const uint4*>(sp + hh * RA_IN_BYTES + 16);
+                  w[8 * hh + 0] = v0.x; w[8 * hh + 1] = v0.y; w[8 * hh + 2] = v0.z; w[8 * hh + 3] = v0.w;
+                  w[8 * hh + 4] = v1.x; w[8 * hh + 5] = v1.y; w[8 * hh + 6] = v1.z; w[8 * hh + 7] = v1.w;
+                } else {
+                  const uint16_t* src = p.g[rr * a + kk];
+#pragma unroll
+                  for (int u = 0; u < RA_EPT; ++u) {
+                    const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
+                    w[8 * hh + (u >> 1)] |= (u & 1) ? (b << 16) : b;
+                  }
+                }
+              }
+              if (++kk == a) {
+                kk = 0;
+                if (++rr == n) rr = 0;
+              }
             }
           }
         }
@@ -289,54 +359,38 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
         rp.next();
       };
 
-      f2_t H[8], L[8];
-      int r = t.owner + 1 == n ? 0 : t.owner + 1;
-      for (int j = 0; j < n; ++j) {
-        const uint16_t* const* gr = p.g + r * a;
-        f2_t h[8], l[8];
-        uint32_t w[8];
-        take(gr[0], w);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          h[u] = bf16x2_to_f2(w[u]);
-          l[u] = 0ull;
-        }
-        for (int k = 1; k < a; ++k) {
-          take(gr[k], w);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const f2_t x = bf16x2_to_f2(w[u]);
-            if (COMP) {
-              f2_t e;
-              h[u] = f2_fast_two_sum(h[u], x, e);   // measured faster here; the rank combine uses TwoSum
-              l[u] = f2_add(l[u], e);
-            } else {
-              h[u] = f2_add(h[u], x);
-            }
+      // Inputs in ring order: rank owner+1 with its micro-steps 0..a-1, then owner+2, ..., owner.  Whole
+      // stages first (two inputs each, no per-input guards), then a last single input when n*a is odd.
+      f2_t H[8], L[8], h[8];
+      auto run = [&](auto full_tag) {
+        int r = t.owner + 1 == n ? 0 : t.owner + 1, k = 0;
+        bool first_rank = true;
+        auto advance = [&]() {
+          if (++k == a) {
+            k = 0;
+            first_rank = false;
+            if (++r == n) r = 0;
           }
+        };
+        int q = 0;
+        for (; q + RA_NPS <= nin; q += RA_NPS) {
+          uint32_t w[8 * RA_NPS];
+          take(full_tag, RA_NPS, r, k, w);
+          fold_input<COMP, 0>(H, L, h, w, q == 0, k == 0, k == a - 1, first_rank);
+          advance();
+          fold_input<COMP, 1>(H, L, h, w, false, k == 0, k == a - 1, first_rank);
+          advance();
         }
-        if (j == 0) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            H[u] = h[u];
-            L[u] = l[u];
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (COMP) {
-              f2_t e;
-              H[u] = f2_two_sum(H[u], h[u], e);
-              L[u] = f2_add(L[u], e);
-              // With one micro-step l is +0 and L is never -0, so L + l == L: the add is skipped.
-              if (a > 1) L[u] = f2_add(L[u], l[u]);
-            } else {
-              H[u] = f2_add(H[u], h[u]);
-            }
-          }
+        if (q < nin) {
+          uint32_t w[8 * RA_NPS];
+          take(full_tag, 1, r, k, w);
+          fold_input<COMP, 0>(H, L, h, w, q == 0, k == 0, k == a - 1, first_rank);
         }
-        if (++r == n) r = 0;
-      }
+      };
+      static_assert(RA_NPS == 2, "the stage loop folds two inputs");
+      // A whole cell is TILE-aligned, so every thread of it is active; t.end <= p8 keeps the tail group out.
+      if (t.end - t.start == TILE && t.end <= p8) run(std::true_type{});
+      else run(std::false_type{});
 
       // gbar = fl(p * inv) for the 16 elements; count the non-finite ones of this tile.
       float o[RA_EPT];
