@@ -12,8 +12,11 @@
 // into a ring of shared-memory stages, bounded mbarrier waits -- with a consumer that keeps the tree as a
 // binary counter: slot l holds the pending sum of a complete block of 2^l ranks, so at most log2(n) partial
 // sums are live, each in registers.  To leave room for them a consumer thread owns 8 elements (the ring
-// kernel's 16), so a stage holds half a tile (3840 elements, a 7.5 KB copy) and the ring has twice the stages.
+// kernel's 16), so a stage input is half a tile (3840 elements, a 7.5 KB copy); plain arithmetic puts four
+// inputs on a stage, compensated one.  Whole half tiles take a loop without per-input guards.
 // rs_tree_kernel: the same tree over the staged per-rank accumulators, one element per thread.
+#include <type_traits>
+
 #include "dp_device.cuh"
 #include "dp_internal.h"
 #include "dp_launch.h"
@@ -25,13 +28,21 @@ constexpr int TT_CWARPS = 15;
 constexpr int TT_CTHREADS = TT_CWARPS * 32;
 constexpr int TT_EPT = 8;                          // elements per consumer thread: one 16-byte shared load
 constexpr int TT_THREADS = TT_CTHREADS + 32;       // + one producer warp
-constexpr int TT_SUB = TT_CTHREADS * TT_EPT;       // elements of a stage: half a tile
-constexpr int TT_STAGES = 24;
-constexpr int TT_STAGE_BYTES = TT_SUB * 2;
-constexpr int TT_SMEM = TT_STAGES * TT_STAGE_BYTES + 2 * TT_STAGES * 8 + 32;
+constexpr int TT_SUB = TT_CTHREADS * TT_EPT;       // elements of a stage input: half a tile
+constexpr int TT_IN_BYTES = TT_SUB * 2;            // one input's half tile: a 7.5 KB bulk copy
+constexpr int TT_RING_BYTES = 24 * TT_IN_BYTES;    // 180 KB of stages in flight
+constexpr int TT_MAX_STAGES = 24;
+constexpr int TT_SMEM = TT_RING_BYTES + 2 * TT_MAX_STAGES * 8 + 32;
 constexpr int RT_LEVELS = 5;                       // staged kernel: slots for n <= 16 (levels 0..4)
-static_assert(TILE == 2 * TT_SUB, "a tile is two stages");
-static_assert(TT_STAGE_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
+// Inputs per stage: four in plain arithmetic; one when the compensated pending sums (hi and lo pairs) take
+// the registers.
+template <int LEVELS, bool COMP>
+__host__ __device__ constexpr int tt_nps() { return COMP ? 1 : 4; }
+template <int LEVELS, bool COMP>
+__host__ __device__ constexpr int tt_stages() { return TT_RING_BYTES / (tt_nps<LEVELS, COMP>() * TT_IN_BYTES); }
+static_assert(TILE == 2 * TT_SUB, "a tile is two half tiles");
+static_assert(TT_IN_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
+static_assert(tt_stages<4, true>() <= TT_MAX_STAGES && tt_stages<4, false>() <= TT_MAX_STAGES, "barriers fit");
 static_assert(TT_SMEM + 64 <= 227 * 1024, "shared memory fits one CTA");
 
 template <int MAXSEG>
@@ -70,16 +81,49 @@ __device__ __forceinline__ Part8 tree_add(const Part8& x, const Part8& y) {
   return z;
 }
 
+template <int NST>
 struct StagePos {
   uint32_t slot = 0, phase = 0, count = 0;
   __device__ __forceinline__ void next() {
     ++count;
-    if (++slot == TT_STAGES) {
+    if (++slot == NST) {
       slot = 0;
       phase ^= 1u;
     }
   }
 };
+
+// Fold input HH of a stage (4 words = 8 bf16 of this thread) into rank r's partial sum `cur` (kfirst: its first
+// micro-step; compensated: Fast2Sum with the error terms in cur.l).  At the rank's last micro-step (klast) the
+// rank is complete: the slots below the lowest clear bit of r are all occupied and merge into it, and that
+// bit's slot takes the sum (static slot indices keep every slot in registers).  When r completes a block of
+// 2^LEVELS ranks, cur is left holding the total.
+template <bool COMP, int LEVELS, int HH, int NW>
+__device__ __forceinline__ void tree_fold(Part8 (&slot)[LEVELS], Part8& cur, const uint32_t (&w)[NW], int r,
+                                          bool kfirst, bool klast) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const f2_t xx = bf16x2_to_f2(w[4 * HH + u]);
+    if (kfirst) {
+      cur.h[u] = xx;
+      cur.l[u] = 0ull;
+    } else if (COMP) {
+      f2_t e;
+      cur.h[u] = f2_fast_two_sum(cur.h[u], xx, e);
+      cur.l[u] = f2_add(cur.l[u], e);
+    } else {
+      cur.h[u] = f2_add(cur.h[u], xx);
+    }
+  }
+  if (klast) {
+    const int top = __ffs(~r) - 1;
+#pragma unroll
+    for (int lv = 0; lv < LEVELS; ++lv) {
+      if (lv < top) cur = tree_add<COMP>(slot[lv], cur);
+      else if (lv == top) slot[lv] = cur;
+    }
+  }
+}
 
 // The stage range of half h of a tile: the tile's elements [lo, hi) in that half, copied as the 8-aligned
 // hull [lo & ~7, min(ceil8(hi), psi & ~7)) -- the buffer's last partial 8 elements are read from global.
@@ -100,22 +144,25 @@ __device__ __forceinline__ Half half_of(const Tile& t, int h) {
 // pending blocks, and a full block of 2^LEVELS ranks is the total itself.
 template <int MAXSEG, bool COMP, int LEVELS>
 __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid_constant__ TreeParams<MAXSEG> p) {
+  constexpr int NPS = tt_nps<LEVELS, COMP>();
+  constexpr int NST = tt_stages<LEVELS, COMP>();
+  constexpr int SBY = NPS * TT_IN_BYTES;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TT_STAGES * TT_STAGE_BYTES);
-  uint64_t* empty = full + TT_STAGES;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + TT_STAGES);
-  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + TT_STAGES + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TT_RING_BYTES);
+  uint64_t* empty = full + NST;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + NST);
+  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + NST + 1);
   __shared__ float s_inv;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = p.n, a = p.a;
+  const int n = p.n, a = p.a, nin = n * a;
   const int ntiles = p.seg.ntiles;
   const int64_t psi = p.seg.psi;
   const int64_t p8 = psi & ~int64_t(7);
 
   if (tid == 0) {
-    for (int s = 0; s < TT_STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), TT_CWARPS);
     }
@@ -141,7 +188,7 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
   if (warp == TT_CWARPS) {
     // ------------------------------------------------------------ producer: inputs in rank order 0..n-1
     if (lane == 0) {
-      StagePos sp;
+      StagePos<NST> sp;
       TileWalker<MAXSEG> walk;
       for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
         const Tile t = walk.at(p.seg, tile);
@@ -151,16 +198,19 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
           int64_t sb = (x.hi + 7) & ~int64_t(7);
           if (sb > p8) sb = p8;
           const uint32_t bytes = sb > x.sa ? (uint32_t)(sb - x.sa) * 2u : 0u;
-          for (int q = 0; q < n * a && !*s_abort; ++q) {
-            if (sp.count >= (uint32_t)TT_STAGES &&
+          for (int q = 0; q < nin && !*s_abort; q += NPS) {
+            if (sp.count >= (uint32_t)NST &&
                 !mbar_wait_bounded(smem_u32(&empty[sp.slot]), sp.phase ^ 1u, p.timeout_ns, s_abort)) {
               if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
               *s_abort = 1;
               break;
             }
+            const int cnt = nin - q < NPS ? nin - q : NPS;
             const uint32_t fb = smem_u32(&full[sp.slot]);
-            mbar_arrive_expect_tx(fb, bytes);
-            if (bytes) bulk_g2s(smem_u32(stages + sp.slot * TT_STAGE_BYTES), p.g[q] + x.sa, bytes, fb);
+            mbar_arrive_expect_tx(fb, bytes * (uint32_t)cnt);
+            if (bytes)
+              for (int hh = 0; hh < cnt; ++hh)
+                bulk_g2s(smem_u32(stages + sp.slot * SBY + hh * TT_IN_BYTES), p.g[q + hh] + x.sa, bytes, fb);
             sp.next();
           }
         }
@@ -168,16 +218,16 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
       // Never leave with copies in flight: wait for the newest issued phase of every slot.
       if (*s_abort) {
         const uint32_t it = sp.count;
-        const uint32_t first = it > (uint32_t)TT_STAGES ? it - TT_STAGES : 0u;
+        const uint32_t first = it > (uint32_t)NST ? it - NST : 0u;
         for (uint32_t y = first; y < it; ++y)
-          (void)mbar_wait_bounded(smem_u32(&full[y % TT_STAGES]), (y / TT_STAGES) & 1u, p.timeout_ns, nullptr);
+          (void)mbar_wait_bounded(smem_u32(&full[y % NST]), (y / NST) & 1u, p.timeout_ns, nullptr);
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers: 8 elements per thread
     const f2_t inv2 = f2_pack(s_inv, s_inv);
-    StagePos sp;
+    StagePos<NST> sp;
     TileWalker<MAXSEG> walk;
     bool live = true;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -189,24 +239,43 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
         const bool active = e0 < x.hi;
         const bool tailgrp = active && (e0 + TT_EPT > p8);
 
-        // One stage: wait for its bytes, take this thread's 8 values, release the slot.
-        auto take = [&](const uint16_t* src, uint32_t (&w)[4]) {
+        // One stage: wait for its bytes, take this thread's 8 values of each of its cnt inputs (input q0 + hh),
+        // release the slot.  whole (a whole half tile below the buffer's last partial 8-group): shared loads
+        // only.  Otherwise inactive threads take zeros and the tail group is read from global memory.
+        auto take = [&](bool whole, int cnt, int q0, uint32_t (&w)[4 * tt_nps<LEVELS, COMP>()]) {
           if (live && !mbar_wait_bounded(smem_u32(&full[sp.slot]), sp.phase, p.timeout_ns, s_abort)) {
             if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
             *s_abort = 1;
             live = false;
           }
+          const unsigned char* src_s = stages + sp.slot * SBY + 2 * TT_EPT * tid;
+          if (whole) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) w[u] = 0u;
-          if (active && live) {
-            if (!tailgrp) {
-              const uint4 v = *reinterpret_cast<const uint4*>(stages + sp.slot * TT_STAGE_BYTES + 2 * TT_EPT * tid);
-              w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-            } else {
+            for (int hh = 0; hh < NPS; ++hh) {
+              if (hh < cnt) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src_s + hh * TT_IN_BYTES);
+                w[4 * hh + 0] = v.x; w[4 * hh + 1] = v.y; w[4 * hh + 2] = v.z; w[4 * hh + 3] = v.w;
+              }
+            }
+          } else {
 #pragma unroll
-              for (int u = 0; u < TT_EPT; ++u) {
-                const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
-                w[u >> 1] |= (u & 1) ? (b << 16) : b;
+            for (int u = 0; u < 4 * NPS; ++u) w[u] = 0u;
+            if (active && live) {
+#pragma unroll
+              for (int hh = 0; hh < NPS; ++hh) {
+                if (hh < cnt) {
+                  if (!tailgrp) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(src_s + hh * TT_IN_BYTES);
+                    w[4 * hh + 0] = v.x; w[4 * hh + 1] = v.y; w[4 * hh + 2] = v.z; w[4 * hh + 3] = v.w;
+                  } else {
+                    const uint16_t* src = p.g[q0 + hh];
+#pragma unroll
+                    for (int u = 0; u < TT_EPT; ++u) {
+                      const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
+                      w[4 * hh + (u >> 1)] |= (u & 1) ? (b << 16) : b;
+                    }
+                  }
+                }
               }
             }
           }
@@ -217,41 +286,36 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
           sp.next();
         };
 
-        Part8 slot[LEVELS], whole, cur;
-        for (int r = 0; r < n; ++r) {
-          uint32_t w[4];
-          take(p.g[r * a], w);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            cur.h[u] = bf16x2_to_f2(w[u]);
-            cur.l[u] = 0ull;
+        // Inputs in rank order, each rank's micro-steps summed before it joins the tree, NPS to a stage (the
+        // last stage takes the remaining nin mod NPS).
+        Part8 slot[LEVELS], cur;
+        const bool whole_half = x.hi - x.lo == TT_SUB && x.hi <= p8;
+        int r = 0, k = 0, q = 0;
+        constexpr int H1 = NPS > 1 ? 1 : 0, H2 = NPS > 2 ? 2 : 0, H3 = NPS > 3 ? 3 : 0;
+        while (q < nin) {
+          const int cnt = nin - q < NPS ? nin - q : NPS;
+          uint32_t w[4 * NPS];
+          take(whole_half, cnt, q, w);
+          tree_fold<COMP, LEVELS, 0>(slot, cur, w, r, k == 0, k == a - 1);
+          if (++k == a) { k = 0; ++r; }
+          if (NPS > 1 && cnt > 1) {
+            tree_fold<COMP, LEVELS, H1>(slot, cur, w, r, k == 0, k == a - 1);
+            if (++k == a) { k = 0; ++r; }
           }
-          for (int k = 1; k < a; ++k) {
-            take(p.g[r * a + k], w);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const f2_t xx = bf16x2_to_f2(w[u]);
-              if (COMP) {
-                f2_t e;
-                cur.h[u] = f2_fast_two_sum(cur.h[u], xx, e);
-                cur.l[u] = f2_add(cur.l[u], e);
-              } else {
-                cur.h[u] = f2_add(cur.h[u], xx);
-              }
-            }
+          if (NPS > 2 && cnt > 2) {
+            tree_fold<COMP, LEVELS, H2>(slot, cur, w, r, k == 0, k == a - 1);
+            if (++k == a) { k = 0; ++r; }
           }
-          // Rank r is complete.  The slots below the lowest clear bit of r are all occupied and merge into
-          // it; that bit's slot takes the sum (static slot indices keep every slot in registers).
-          const int top = __ffs(~r) - 1;
-#pragma unroll
-          for (int lv = 0; lv < LEVELS; ++lv) {
-            if (lv < top) cur = tree_add<COMP>(slot[lv], cur);
-            else if (lv == top) slot[lv] = cur;
+          if (NPS > 3 && cnt > 3) {
+            tree_fold<COMP, LEVELS, H3>(slot, cur, w, r, k == 0, k == a - 1);
+            if (++k == a) { k = 0; ++r; }
           }
-          if (top == LEVELS) whole = cur;
+          q += cnt;
         }
-        // Blocks left without a partner, smallest first, each joining the one below it on the left.
-        Part8 tot = whole;
+
+        // n = 2^LEVELS: the last rank completed the whole block and cur holds the total.  Otherwise the blocks
+        // left without a partner join, smallest first, each the one below it on the left.
+        Part8 tot = cur;
         if (n != (1 << LEVELS)) {
           bool have = false;
 #pragma unroll
