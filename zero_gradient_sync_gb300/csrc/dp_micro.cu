@@ -10,13 +10,12 @@
 // accumulator adds p_k as (H, e) = TwoSum(A_H, p_H), A_L = (A_L + e) + p_L; gbar uses A_H + A_L.
 //
 // One launch per micro-step, streaming its n bf16 inputs once with 16-byte loads (8 elements a thread,
-// ranks in batches of four so 4 loads are in flight besides the accumulator's) and reading / writing the
+// ranks in batches of eight, issued together with the accumulator's loads) and reading / writing the
 // accumulator at the owner's local index.  The last micro-step's launch writes gbar instead, counts
 // non-finite values and publishes the skip decision and t like pass A of the step.
 //
 // With one micro-step (a = 1) the per-micro-step order is the step's own ring order, operation for
-// operation, so the same kernel also serves as pass A of dp_step for a = 1: with few inputs per tile it
-// streams faster than the bulk-copy pipeline, whose per-stage overhead is then spread over too little work.
+// operation: the same result as dp_step's pass A, which runs on the ring kernel.
 #include "dp_device.cuh"
 #include "dp_internal.h"
 #include "dp_launch.h"
@@ -86,6 +85,39 @@ __global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_const
     const int64_t A = t.start & ~int64_t(7), B = (t.end + 7) & ~int64_t(7);
     const int64_t delta = t.loff - t.goff;
     for (int64_t e0 = A + RM_EPT * (int64_t)threadIdx.x; e0 < B; e0 += RM_EPT * RM_THREADS) {
+      // The shard accumulator at the owner's local index: the group's elements inside the tile.  Its loads
+      // are issued first, so they are in flight together with the gradients'.
+      const bool whole = e0 >= t.start && e0 + RM_EPT <= t.end;
+      float* accp = p.acc[t.owner];
+      const int64_t j = delta + e0;   // local index of element e0 (only elements inside the tile are touched)
+      float ah[RM_EPT], al[RM_EPT];
+      if (!FIRST) {
+        const bool vec = whole && (((reinterpret_cast<uintptr_t>(accp + (COMP ? 2 * j : j))) & 15) == 0);
+        if (vec) {
+          if (COMP) {
+#pragma unroll
+            for (int q = 0; q < RM_EPT / 2; ++q) {
+              const float4 v = *reinterpret_cast<const float4*>(accp + 2 * (j + 2 * q));
+              ah[2 * q] = v.x; al[2 * q] = v.y; ah[2 * q + 1] = v.z; al[2 * q + 1] = v.w;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < RM_EPT / 4; ++q) {
+              const float4 v = *reinterpret_cast<const float4*>(accp + j + 4 * q);
+              ah[4 * q] = v.x; ah[4 * q + 1] = v.y; ah[4 * q + 2] = v.z; ah[4 * q + 3] = v.w;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < RM_EPT; ++u) {
+            ah[u] = al[u] = 0.0f;
+            if (e0 + u >= t.start && e0 + u < t.end) {
+              ah[u] = COMP ? accp[2 * (j + u)] : accp[j + u];
+              if (COMP) al[u] = accp[2 * (j + u) + 1];
+            }
+          }
+        }
+      }
       // p_k for these 8 elements: the ranks in ring order s+1, ..., s.
       f2_t H[4], L[4];
       int r = t.owner + 1 == n ? 0 : t.owner + 1;
@@ -121,10 +153,6 @@ __global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_const
         }
         r = rr;
       }
-      // The shard accumulator at the owner's local index: the group's elements inside the tile.
-      const bool whole = e0 >= t.start && e0 + RM_EPT <= t.end;
-      float* accp = p.acc[t.owner];
-      const int64_t j = delta + e0;   // local index of element e0 (only elements inside the tile are touched)
       float hv[RM_EPT], lv[RM_EPT];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -133,32 +161,6 @@ __global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_const
       }
       if (!FIRST) {
         // A += p
-        float ah[RM_EPT], al[RM_EPT];
-        const bool vec = whole && (((reinterpret_cast<uintptr_t>(accp + (COMP ? 2 * j : j))) & 15) == 0);
-        if (vec) {
-          if (COMP) {
-#pragma unroll
-            for (int q = 0; q < RM_EPT / 2; ++q) {
-              const float4 v = *reinterpret_cast<const float4*>(accp + 2 * (j + 2 * q));
-              ah[2 * q] = v.x; al[2 * q] = v.y; ah[2 * q + 1] = v.z; al[2 * q + 1] = v.w;
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < RM_EPT / 4; ++q) {
-              const float4 v = *reinterpret_cast<const float4*>(accp + j + 4 * q);
-              ah[4 * q] = v.x; ah[4 * q + 1] = v.y; ah[4 * q + 2] = v.z; ah[4 * q + 3] = v.w;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < RM_EPT; ++u) {
-            ah[u] = al[u] = 0.0f;
-            if (e0 + u >= t.start && e0 + u < t.end) {
-              ah[u] = COMP ? accp[2 * (j + u)] : accp[j + u];
-              if (COMP) al[u] = accp[2 * (j + u) + 1];
-            }
-          }
-        }
 #pragma unroll
         for (int u = 0; u < RM_EPT; ++u) {
           if (COMP) {
