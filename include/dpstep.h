@@ -74,7 +74,9 @@ typedef enum {
 
 /* Reduction arithmetic, the low 4 bits of every sum_mode argument. */
 enum {
-  DP_SUM_COMPENSATED = 0, /* fp32 with Knuth's TwoSum error terms carried alongside */
+  DP_SUM_COMPENSATED = 0, /* fp32 with Knuth's TwoSum error terms carried alongside; in the
+                             ring order of dp_step / dp_step_reduce one (hi, lo) pair is carried
+                             through all n*a inputs, (hi, e) = TwoSum(hi, x), lo = lo + e */
   DP_SUM_PLAIN = 1        /* plain fp32 additions */
 };
 
@@ -266,8 +268,9 @@ dp_status_t dp_reduce_scatter_avg(float* const* gbar_shard, const float* const* 
  *   gbar_shard[s][local] = fl32(A * fl32(1 / (n S)))   (written by the k = a-1 call)
  * Compensated mode carries TwoSum error terms in both sums ((H, e) =
  * TwoSum(A_H, p_H), A_L = (A_L + e) + p_L) and ends with A_H + A_L.  This
- * order differs from dp_step's (micro-steps summed within a rank first), so
- * results agree with it to rounding, not bit for bit.  The k = a-1 call also
+ * order differs from dp_step's (all of a rank's micro-steps before the next
+ * rank), so results agree with it to rounding, not bit for bit (for a = 1 the
+ * two perform the same operations).  The k = a-1 call also
  * counts non-finite gbar values and, like dp_step_reduce, publishes found_inf
  * and advances t and the beta powers unless found.
  * g: n device pointers, micro-step k of every rank, each psi bf16.
@@ -300,11 +303,14 @@ dp_status_t dp_allgather_params(uint16_t* const* replicas, const float* const* m
 /* The fused step: dp_step_reduce then dp_step_update (two kernels).
  * grads: host array of n*a device pointers, rank-major (grads[r*a + k] is
  * micro-step k of rank r), each psi bf16.  Per element the gradient is summed
- * in a fixed order -- micro-steps k = 0..a-1 within each rank, then ranks in
- * ring order s+1, ..., s for the owner s (or in the tree order of
- * DP_ORDER_TREE) -- so results are bit-identical run to run and identical to
- * dp_accumulate + dp_reduce_scatter_avg + dp_adam_shard + dp_allgather_params
- * with the same sum_mode.  gbar_shard: n device shards of dp_shard_len floats, or
+ * in a fixed order -- ranks in ring order s+1, ..., s for the owner s, each
+ * rank's micro-steps k = 0..a-1 (or in the tree order of DP_ORDER_TREE) -- so
+ * results are bit-identical run to run.  Plain: each rank's micro-steps are
+ * summed first, then the ranks' sums, exactly as dp_accumulate +
+ * dp_reduce_scatter_avg + dp_adam_shard + dp_allgather_params compute it.
+ * Compensated (ring order): one (hi, lo) pair through all n*a inputs, which
+ * agrees with the staged calls (one pair per rank, then the ranks' pairs) to
+ * rounding.  gbar_shard: n device shards of dp_shard_len floats, or
  * NULL to carve them from ws (dp_workspace_size bytes, 256-byte aligned).
  * If any reduced value is not finite (or a wait timed out) master, m, v,
  * replicas and t are left bit-for-bit unchanged. */

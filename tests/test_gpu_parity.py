@@ -139,6 +139,24 @@ def test_reduction_order_matches_ring_simulation(dev, mode, arith):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("mode,arith", [(PLAIN, "f32"), (COMP, "f32chain")])
+@pytest.mark.parametrize("n,a,layout", [(3, 3, "even"), (3, 1, "ragged"), (1, 1, "even"), (7, 1, "random")])
+def test_odd_input_count_matches_ring_simulation(dev, mode, arith, n, a, layout):
+    """Pass A streams two inputs a stage; with n*a odd the last stage of every tile carries one.  Many whole
+    tiles (the guard-free loop) plus segment edges and a ragged buffer tail (the general loop): gbar equals the
+    simulated ring bit for bit, and the step matches the oracle."""
+    wl = BASE.with_(psi=7680 * 23 + 13, n=n, a=a, stage=1, layout=layout, nseg=5, seed=61 + n + a, sigma_g=1e-2,
+                    tail_p=0.02, tail_mult=1e3, loss_scale=4.0)
+    c = gu.make_case(wl)
+    b = gu.upload(c)
+    b.step(adam_of(wl), wl.loss_scale, mode)
+    torch.cuda.synchronize()
+    ref = brute.ring_gbar(c.grads, wl.n, wl.a, c.segs, wl.psi, wl.loss_scale, arith)
+    got = sd.gather_full(b.gbar, c.segs, wl.psi, 1)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    gu.assert_matches_oracle(gu.gpu_result(c, b), gu.run_oracle(c))
+
+
 def test_compensated_gbar_is_nearly_exact(dev):
     """Compensated reduction: gbar within 1 ulp of the exactly rounded average (n S a power of two)."""
     wl = synth.WORKLOADS["llama7b_16l"].with_(psi=300_000, a=8, seed=8)
