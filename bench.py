@@ -405,7 +405,8 @@ def native_main(args, wl):
                                ("reduce_tree" if tree else "reduce"))
 
     # End to end through the public call with host buffers: the step's gradients copied from pinned host
-    # memory, the step, and the step's status read back, every step.
+    # memory, the step, and the step's status read back, every step -- for the two-pass step one C-ABI call,
+    # dp_step_from_host, does all three.
     e2e = None
     if not args.no_e2e:
         KE = args.e2e_steps or min(K, 20)
@@ -414,14 +415,15 @@ def native_main(args, wl):
         s1 = torch.cuda.Event(enable_timing=True)
 
         def e2e_step():
+            if not single and not micro:
+                bufs.step_from_host(host_grads, A, wl.loss_scale, mode, host_state=host_state)
+                return
             for q, h in enumerate(host_grads):
                 bufs.grads[q].view(torch.int16).copy_(h, non_blocking=True)
             if single:
                 bufs.step_single_pass(A, wl.loss_scale, mode)
-            elif micro:
-                bufs.step_micro(A, wl.loss_scale, mode)
             else:
-                bufs.step(A, wl.loss_scale, mode)
+                bufs.step_micro(A, wl.loss_scale, mode)
             host_state.copy_(bufs.state, non_blocking=True)
 
         # Untimed warm-up of this leg too: the first host-to-device copy from freshly pinned pages has measured

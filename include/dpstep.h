@@ -319,6 +319,24 @@ dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* cons
                     float loss_scale, int32_t sum_mode, float* const* gbar_shard, void* ws,
                     dp_step_state_t* d_state, dp_stream_t stream);
 
+/* dp_step with the step's gradients in host memory: the end-to-end call of a
+ * loop whose gradients arrive on the host.  On `stream`, in order: the n*a
+ * host buffers host_grads[q] (psi bf16 each, rank-major like grads) are
+ * copied into the caller's device buffers grads[q] (one cudaMemcpyAsync
+ * each), dp_step runs on them, and, if host_state is not NULL, the 64-byte
+ * step state is copied back to host_state (read found_inf / t there after a
+ * stream synchronize).  Every argument is checked before anything is
+ * queued; results are those of dp_step on the same gradients.  host_grads
+ * and host_state should be pinned (cudaHostAlloc / cudaHostRegister) for the
+ * copies to be asynchronous and run at the link's rate; they must stay valid
+ * until the stream has passed the copies.  Errors: those of dp_step, and
+ * DP_ERR_CUDA if a copy cannot be queued. */
+dp_status_t dp_step_from_host(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                              const uint16_t* const* host_grads, uint16_t* const* grads, int32_t a,
+                              const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
+                              float* const* gbar_shard, void* ws, dp_step_state_t* d_state,
+                              dp_step_state_t* host_state, dp_stream_t stream);
+
 /* First half of dp_step (one kernel): accumulate + ring reduce-scatter +
  * average + unscale + non-finite check, gbar into the shards; the last CTA
  * publishes found_inf / nonfinite and, unless found, advances t and the

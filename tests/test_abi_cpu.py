@@ -132,6 +132,30 @@ def test_step_argument_errors_launch_nothing(dp):
     assert dp.dp_kernel_launches() == before
 
 
+def test_step_from_host_argument_errors_queue_nothing(dp):
+    """dp_step_from_host checks every argument before it queues a copy or a kernel (no GPU needed)."""
+    import ctypes
+    L = dp.Layout(1, 2, 16, [(0, 8, 0, 0), (8, 8, 1, 0)])
+    arr = ctypes.c_void_p * 2
+    fake, null = arr(16, 32), arr(0, 0)
+    A = dp.adam()
+    f = dp.LIB.dp_step_from_host
+    before = dp.dp_kernel_launches()
+    # a = 0
+    assert f(fake, fake, fake, fake, fake, fake, 0, ctypes.byref(L.c), A, 1.0, 0, fake, None, 256, None,
+             None) == dp.DP_ERR_INVALID_ARG
+    # a host gradient buffer missing
+    assert f(fake, fake, fake, fake, null, fake, 1, ctypes.byref(L.c), A, 1.0, 0, fake, None, 256, None,
+             None) != dp.DP_OK
+    # a misaligned device gradient buffer
+    assert f(fake, fake, fake, fake, fake, arr(16, 17), 1, ctypes.byref(L.c), A, 1.0, 0, fake, None, 256, None,
+             None) == dp.DP_ERR_ALIGNMENT
+    # no state
+    assert f(fake, fake, fake, fake, fake, fake, 1, ctypes.byref(L.c), A, 1.0, 0, fake, None, None, None,
+             None) == dp.DP_ERR_INVALID_ARG
+    assert dp.dp_kernel_launches() == before
+
+
 def test_global_batch(dp):
     G = json.load(open(os.path.join(ROOT, "tests", "golden", "pages_numbers.json")))["global_batch_example"]
     assert dp.dp_global_batch(G["b"], G["n"], G["a"]) == G["B_global"] == 256

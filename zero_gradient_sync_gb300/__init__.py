@@ -11,5 +11,5 @@ from ._lib import (  # noqa: F401
     Layout, adam, dp_accumulate, dp_adam_shard, dp_allgather_params, dp_checkpoint_info, dp_checkpoint_load,
     dp_checkpoint_save, dp_get_wait_timeout_ns, dp_global_batch, dp_kernel_launches, dp_memory_model,
     dp_read_status, dp_reduce_scatter_avg, dp_reduce_scatter_micro, dp_scaler_init, dp_selftest_wait_timeout, dp_set_wait_timeout_ns,
-    dp_state_init, dp_step, dp_step_reduce, dp_step_scaled, dp_step_single_pass, dp_step_static, dp_step_update,
+    dp_state_init, dp_step, dp_step_from_host, dp_step_reduce, dp_step_scaled, dp_step_single_pass, dp_step_static, dp_step_update,
     dp_traffic_model, new_state, read_state, scaler)

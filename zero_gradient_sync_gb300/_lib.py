@@ -80,6 +80,8 @@ def _load() -> ctypes.CDLL:
         "dp_allgather_params": (c_i32, [c_vp, c_vp, P(dp_layout_t), c_vp, c_vp]),
         "dp_step": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32, c_vp,
                             c_vp, c_vp, c_vp]),
+        "dp_step_from_host": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32,
+                                      c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
         "dp_step_reduce": (c_i32, [c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t, c_f32, c_i32, c_vp, c_vp]),
         "dp_step_update": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, P(dp_layout_t), dp_adam_t, c_vp, c_vp]),
         "dp_read_status": (c_i32, [c_vp, P(c_i32), P(c_i32), c_vp]),
@@ -264,6 +266,34 @@ def dp_step(replicas, master, m, v, grads, a: int, layout: Layout, adam_: dp_ada
     _check(LIB.dp_step(_ptr_array(replicas), _ptr_array(master), _ptr_array(m), _ptr_array(v), _ptr_array(grads), a,
                        ctypes.byref(layout.c), adam_, loss_scale, sum_mode, gb, w, _ptr(state), _stream(stream)),
            "dp_step")
+
+
+def dp_step_from_host(replicas, master, m, v, host_grads, grads, a: int, layout: Layout, adam_: dp_adam_t,
+                      loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED, gbar_shard=None, ws=None, state=None,
+                      host_state=None, stream=None) -> None:
+    """dp_step with the gradients in host memory: host_grads (CPU tensors, pinned for asynchronous copies, 2-byte
+    elements) are copied into the device buffers grads on the stream, then the step runs; host_state (a CPU
+    uint8 tensor of STATE_BYTES, or None) receives the step state afterwards."""
+    lens = layout.state_lens()
+    for name, ts in (("master", master), ("m", m), ("v", v)):
+        _check_tensors(ts, 4, lens, name)
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    _check_tensors(grads, 2, [layout.psi] * len(grads), "grads")
+    if len(host_grads) != len(grads):
+        raise ValueError("host_grads: %d buffers for %d device buffers" % (len(host_grads), len(grads)))
+    for i, h in enumerate(host_grads):
+        if h.is_cuda or h.element_size() != 2 or not h.is_contiguous() or h.numel() < layout.psi:
+            raise ValueError("host_grads[%d] must be a contiguous CPU tensor of >= psi 2-byte elements" % i)
+    hs = 0
+    if host_state is not None:
+        if host_state.is_cuda or host_state.numel() * host_state.element_size() < STATE_BYTES:
+            raise ValueError("host_state must be a CPU tensor of at least %d bytes" % STATE_BYTES)
+        hs = host_state.data_ptr()
+    hp = (c_vp * max(1, len(host_grads)))(*[h.data_ptr() for h in host_grads])
+    gb, w = _gbar_args(layout, gbar_shard, ws)
+    _check(LIB.dp_step_from_host(_ptr_array(replicas), _ptr_array(master), _ptr_array(m), _ptr_array(v), hp,
+                                 _ptr_array(grads), a, ctypes.byref(layout.c), adam_, loss_scale, sum_mode, gb, w,
+                                 _ptr(state), hs, _stream(stream)), "dp_step_from_host")
 
 
 def dp_step_reduce(gbar_shard, ws, grads, a: int, layout: Layout, adam_: dp_adam_t, loss_scale: float,

@@ -71,6 +71,13 @@ class StepBuffers:
         _lib.dp_step(self.replicas, self.master, self.m, self.v, self.grads, self.a, self.layout, adam_,
                      loss_scale, sum_mode, gbar_shard=self.gbar, state=self.state, stream=stream)
 
+    def step_from_host(self, host_grads, adam_: _lib.dp_adam_t, loss_scale: float,
+                       sum_mode: int = DP_SUM_COMPENSATED, host_state=None, stream=None) -> None:
+        """One step with this step's gradients in host memory (copied into self.grads first)."""
+        _lib.dp_step_from_host(self.replicas, self.master, self.m, self.v, host_grads, self.grads, self.a,
+                               self.layout, adam_, loss_scale, sum_mode, gbar_shard=self.gbar, state=self.state,
+                               host_state=host_state, stream=stream)
+
     def step_scaled(self, adam_: _lib.dp_adam_t, scaler_: _lib.dp_scaler_t, sum_mode: int = DP_SUM_COMPENSATED,
                     stream=None) -> None:
         _lib.dp_step_scaled(self.replicas, self.master, self.m, self.v, self.grads, self.a, self.layout, adam_,

@@ -508,6 +508,43 @@ dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* cons
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
 }
 
+dp_status_t dp_step_from_host(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                              const uint16_t* const* host_grads, uint16_t* const* grads, int32_t a,
+                              const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
+                              float* const* gbar_shard, void* ws, dp_step_state_t* d_state,
+                              dp_step_state_t* host_state, dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  StepScalars s;
+  float* gb[DP_MAX_N];
+  // Every argument is checked before anything is queued, as for dp_step.
+  if ((st = prepare_reduce(P, (const uint16_t* const*)grads, a, adam, loss_scale, sum_mode, gbar_shard, ws, d_state,
+                           s, gb)) != DP_OK)
+    return st;
+  if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)host_grads, P.n * a, "host_grads")) != DP_OK) return st;
+  const cudaStream_t cs = (cudaStream_t)stream;
+  const size_t bytes = (size_t)P.psi * sizeof(uint16_t);
+  if (bytes) {
+    for (int q = 0; q < P.n * a; ++q) {
+      const cudaError_t e = cudaMemcpyAsync(grads[q], host_grads[q], bytes, cudaMemcpyHostToDevice, cs);
+      if (e != cudaSuccess) return cuda_fail(e, "gradient copy to the device");
+    }
+  }
+  LaunchCount lc;
+  cudaError_t e = launch_pass_a(P, (const uint16_t* const*)grads, a, gb, s, d_state, cs, &lc.n);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
+  e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, cs, &lc.n);
+  if (e != cudaSuccess) return cuda_fail(e, "update launch");
+  if (host_state) {
+    e = cudaMemcpyAsync(host_state, d_state, sizeof(dp_step_state_t), cudaMemcpyDeviceToHost, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy to the host");
+  }
+  return DP_OK;
+}
+
 dp_status_t dp_scaler_init(dp_step_state_t* d_state, float scale, dp_stream_t stream) {
   dp_status_t st = check_state(d_state);
   if (st != DP_OK) return st;
