@@ -35,14 +35,18 @@ constexpr int RA_NPS = 2;                      // inputs per stage: two 15 KB bu
 constexpr int RA_IN_BYTES = TILE * 2;          // one tile of one bf16 input
 constexpr int RA_STAGE_BYTES = RA_NPS * RA_IN_BYTES;
 constexpr int RA_GBAR_FLOATS = TILE + 16;      // single pass: the tile's gbar (+16: last group's overhang)
-constexpr int RA_EXTRA_FUSED = RA_GBAR_FLOATS * 4 + TILE * 2;   // + the tile's bf16 staging
-// 180 KB of stages in flight; the single pass gives one stage up for its gbar and staging tiles.
+// Single pass: + the tile's bf16 staging and its master/m/v (fetched while its gradients stream).
+constexpr int RA_STATE_FLOATS = TILE + 16;
+constexpr int RA_EXTRA_FUSED = RA_GBAR_FLOATS * 4 + TILE * 2 + 3 * RA_STATE_FLOATS * 4;
+// 180 KB of stages in flight; the single pass keeps 90 KB and uses the rest for the tile's gbar, staging and
+// optimizer state.
 template <bool FUSED>
-__host__ __device__ constexpr int ra_stages() { return FUSED ? 5 : 6; }
+__host__ __device__ constexpr int ra_stages() { return FUSED ? 3 : 6; }
 template <bool FUSED>
 __host__ __device__ constexpr int ra_bar_offset() { return ra_stages<FUSED>() * RA_STAGE_BYTES + (FUSED ? RA_EXTRA_FUSED : 0); }
+// Barriers: full/empty per stage, the single pass's state full/empty, abort, count.
 template <bool FUSED>
-__host__ __device__ constexpr int ra_smem() { return ra_bar_offset<FUSED>() + 2 * ra_stages<FUSED>() * 8 + 32; }
+__host__ __device__ constexpr int ra_smem() { return ra_bar_offset<FUSED>() + 2 * ra_stages<FUSED>() * 8 + (FUSED ? 16 : 0) + 32; }
 static_assert(ra_smem<true>() + 64 <= 227 * 1024, "single-pass shared memory fits one CTA");
 static_assert(ra_smem<false>() + 64 <= 227 * 1024, "shared memory fits one CTA");
 static_assert(TILE == RA_CTHREADS * RA_EPT, "one 16-element group per consumer thread");
@@ -99,7 +103,7 @@ __device__ __forceinline__ void stage_bf16x4(uint16_t* sb, int64_t off, uint32_t
 // old state from set `cur`, new state into the other set, bf16 of the new master into the staging tile.
 template <int MAXSEG>
 __device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, const Tile& t, const AdamK& K, int cur,
-                                             const float* s_g, uint16_t* s_stage, int tid) {
+                                             const float* s_g, uint16_t* s_stage, const float* s_state, int tid) {
   constexpr int UG = 2;
   const int64_t delta = t.loff - t.goff;
   const int64_t cb = (t.start / TILE) * TILE;
@@ -120,9 +124,10 @@ __device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, cons
       const int gq = base + tid + u * RA_CTHREADS;
       if (gq < ngr) {
         const int64_t jj = jlo + 4 * (int64_t)gq;
-        t4[u] = *reinterpret_cast<const float4*>(M + jj);
-        m4[u] = *reinterpret_cast<const float4*>(Mm + jj);
-        v4[u] = *reinterpret_cast<const float4*>(Vv + jj);
+        // The 4-aligned interior [jlo, jhi) of the old state sits in shared memory (bulk-copied by the producer).
+        t4[u] = *reinterpret_cast<const float4*>(s_state + 4 * gq);
+        m4[u] = *reinterpret_cast<const float4*>(s_state + RA_STATE_FLOATS + 4 * gq);
+        v4[u] = *reinterpret_cast<const float4*>(s_state + 2 * RA_STATE_FLOATS + 4 * gq);
         const float* gs = s_g + (jj - delta - cb);
         g4[u] = galign ? *reinterpret_cast<const float4*>(gs) : make_float4(gs[0], gs[1], gs[2], gs[3]);
       }
@@ -195,10 +200,14 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
   unsigned char* stages = smem;
   float* s_g = reinterpret_cast<float*>(smem + NST * RA_STAGE_BYTES);
   uint16_t* s_stage = reinterpret_cast<uint16_t*>(smem + NST * RA_STAGE_BYTES + RA_GBAR_FLOATS * 4);
+  // single pass: the tile's master, m, v (4-aligned local interior), RA_STATE_FLOATS apart
+  float* s_state = reinterpret_cast<float*>(smem + NST * RA_STAGE_BYTES + RA_GBAR_FLOATS * 4 + TILE * 2);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ra_bar_offset<FUSED>());
   uint64_t* empty = full + NST;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + NST);
-  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + NST + 1);
+  uint64_t* sfull = empty + NST;        // single pass: the tile's state has landed (producer + bytes)
+  uint64_t* sempty = sfull + 1;         // single pass: the update is done reading it (consumer warps)
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sfull + (FUSED ? 2 : 0));
+  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(sfull + (FUSED ? 2 : 0) + 1);
   __shared__ float s_inv;
   __shared__ float s_k[2];
   __shared__ int s_cur;
@@ -213,6 +222,10 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), RA_CWARPS);
+    }
+    if (FUSED) {
+      mbar_init(smem_u32(sfull), 1);
+      mbar_init(smem_u32(sempty), RA_CWARPS);
     }
     *s_abort = 0;
     *s_count = 0ull;
@@ -246,12 +259,36 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
       RingPos<NST> rp;
       TileWalker<MAXSEG> walk;
       const int nin = n * a;
+      uint32_t sit = 0;   // single pass: tiles whose state copies were issued
       for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
         const Tile t = walk.at(p.seg, tile);
         const int64_t A = t.start & ~int64_t(7);
         int64_t B = (t.end + 7) & ~int64_t(7);
         if (B > p8) B = p8;
         const uint32_t bytes = B > A ? (uint32_t)(B - A) * 2u : 0u;
+        // Single pass: the tile's old master/m/v (4-aligned local interior, the current set) into s_state, once
+        // the update of the previous tile has read it.  Issued after the tile's first NST stages, when the next
+        // stage would wait for the consumers anyway.
+        auto issue_state = [&]() {
+          if (sit > 0 && !mbar_wait_bounded(smem_u32(sempty), (sit - 1) & 1u, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+            *s_abort = 1;
+            return;
+          }
+          const int64_t delta = t.loff - t.goff;
+          const int64_t jlo = (t.start + delta + 3) & ~int64_t(3), jhi = (t.end + delta) & ~int64_t(3);
+          const uint32_t sb = jhi > jlo ? (uint32_t)(jhi - jlo) * 4u : 0u;
+          mbar_arrive_expect_tx(smem_u32(sfull), 3u * sb);
+          if (sb) {
+            bulk_g2s(smem_u32(s_state), p.st_master[s_cur][t.owner] + jlo, sb, smem_u32(sfull));
+            bulk_g2s(smem_u32(s_state + RA_STATE_FLOATS), p.st_m[s_cur][t.owner] + jlo, sb, smem_u32(sfull));
+            bulk_g2s(smem_u32(s_state + 2 * RA_STATE_FLOATS), p.st_v[s_cur][t.owner] + jlo, sb, smem_u32(sfull));
+          }
+          ++sit;
+        };
+        const int tile_stages = (nin + RA_NPS - 1) / RA_NPS;
+        const int state_after = tile_stages < NST ? tile_stages : NST;
+        int sq = 0;
         // Inputs in ring order: rank owner+1 first, its micro-steps 0..a-1, then the next rank; two per stage.
         int r = t.owner + 1 == n ? 0 : t.owner + 1, k = 0;
         for (int q = 0; q < nin && !*s_abort; q += RA_NPS) {
@@ -273,8 +310,12 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
             }
           }
           rp.next();
+          if (FUSED && ++sq == state_after) issue_state();
         }
       }
+      // Single pass: never leave with state copies in flight either.
+      if (FUSED && *s_abort && sit > 0)
+        (void)mbar_wait_bounded(smem_u32(sfull), (sit - 1) & 1u, p.timeout_ns, nullptr);
       // Never leave with copies in flight: wait for the newest issued phase of every slot.
       if (*s_abort) {
         const uint32_t it = rp.count;
@@ -291,6 +332,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
     RingPos<NST> rp;
     TileWalker<MAXSEG> walk;
     bool live = true;
+    uint32_t sit_c = 0;   // single pass: tiles whose state this thread has used
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const Tile t = walk.at(p.seg, tile);
       const int64_t A = t.start & ~int64_t(7);
@@ -420,8 +462,19 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
         K.b1 = p.b1f; K.b2 = p.b2f; K.omb1 = p.omb1; K.omb2 = p.omb2; K.eps = p.eps;
         K.step = s_k[0];
         K.rsbc2 = s_k[1];
-        fused_update(p, t, K, s_cur, s_g, s_stage, tid);
+        // The tile's old state, bulk-copied by the producer while the gradients streamed.
+        if (live && !mbar_wait_bounded(smem_u32(sfull), sit_c & 1u, p.timeout_ns, s_abort)) {
+          if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+          *s_abort = 1;
+          live = false;
+        }
+        fused_update(p, t, K, s_cur, s_g, s_stage, s_state, tid);
+        // Order this thread's reads of s_state (and writes of s_stage) before the async proxy's next use of
+        // them, then hand s_state back to the producer.
         fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sempty));
+        ++sit_c;
         named_bar_sync(1, RA_CTHREADS);
         // All-gather: the staged bf16 tile into every replica (16-byte-aligned interior by bulk copies).
         const int64_t ilo = (t.start + 7) & ~int64_t(7), ihi = t.end & ~int64_t(7);
