@@ -96,10 +96,12 @@ def warm_state_by_oracle(b, wl, segs):
     b.state.copy_(torch.frombuffer(bytearray(gu.state_bytes(1, wl.beta1, wl.beta2)), dtype=torch.uint8))
 
 
-def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0, mode=dp.DP_SUM_COMPENSATED):
+def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0, mode=dp.DP_SUM_COMPENSATED,
+                 single=False):
+    """single: dp_step_single_pass (two state sets, the step's results in the set it makes current)."""
     segs = synth.layout_of(wl)
     L = dp.Layout(wl.stage, wl.n, wl.psi, segs)
-    b = StepBuffers(L, wl.a)
+    b = StepBuffers(L, wl.a, second_set=single)
     sd.fill_grads(b.grads, wl)
     t0 = 0
     if warm:
@@ -108,8 +110,15 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0, mode=d
     else:
         sd.fill_master(b.master, wl, segs, wl.stage)
     A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
-    b.reduce(A, wl.loss_scale, mode)
-    b.update(A)
+
+    def step():
+        if single:
+            b.step_single_pass(A, wl.loss_scale, mode)
+        else:
+            b.reduce(A, wl.loss_scale, mode)
+            b.update(A)
+
+    step()
     torch.cuda.synchronize()
     st = dp.read_state(b.state)
     assert (st["found_inf"], st["nonfinite"], st["error"], st["t"]) == (0, 0, 0, t0 + 1)
@@ -122,15 +131,16 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0, mode=d
         o = oracle_at(wl, idx)
     assert (o["found"], o["nonfinite"], o["t"]) == (0, 0, t0 + 1)
     gi = torch.from_numpy(idx).to(b.grads[0].device)
-    g = {"master": gather_state(b.master, segs, idx, wl.stage), "m": gather_state(b.m, segs, idx, wl.stage),
-         "v": gather_state(b.v, segs, idx, wl.stage),
+    cm, cmm, cv = b.current() if single else (b.master, b.m, b.v)
+    g = {"master": gather_state(cm, segs, idx, wl.stage), "m": gather_state(cmm, segs, idx, wl.stage),
+         "v": gather_state(cv, segs, idx, wl.stage),
          "replicas": [sd.bits_of_bf16(r[gi]) for r in b.replicas]}
     gu.assert_close_f32(g["master"], o["master"], "master")
     gu.assert_close_f32(g["m"], o["m"], "m")
     gu.assert_close_f32(g["v"], o["v"], "v")
     gu.assert_replicas(g["replicas"], o["replicas"])
 
-    if repeat:
+    if repeat and not single:
         # the fixed-order reduction is bit-identical run to run over the whole parameter space
         first = [x.clone() for x in b.gbar]
         for _ in range(repeat):
@@ -144,14 +154,13 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0, mode=d
         # one +inf in one rank's micro-step at a seeded element: the whole step is skipped
         r, k, i, _ = synth.inject_site(wl, 0)
         b.grad(r, k)[i:i + 1].view(torch.int16).fill_(synth.BF16_POS_INF)
-        before = [gather_state(x, segs, idx, wl.stage) for x in (b.master, b.m, b.v)]
+        before = [gather_state(x, segs, idx, wl.stage) for x in (b.current() if single else (b.master, b.m, b.v))]
         reps_before = [sd.bits_of_bf16(x[gi]) for x in b.replicas]
-        b.reduce(A, wl.loss_scale, mode)
-        b.update(A)
+        step()
         torch.cuda.synchronize()
         st2 = dp.read_state(b.state)
-        assert (st2["found_inf"], st2["nonfinite"], st2["t"]) == (1, 1, t0 + 1 + repeat)
-        after = [gather_state(x, segs, idx, wl.stage) for x in (b.master, b.m, b.v)]
+        assert (st2["found_inf"], st2["nonfinite"], st2["t"]) == (1, 1, t0 + 1 + (0 if single else repeat))
+        after = [gather_state(x, segs, idx, wl.stage) for x in (b.current() if single else (b.master, b.m, b.v))]
         for x, y in zip(before, after):
             assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
         for x, rep in zip(reps_before, b.replicas):
@@ -180,6 +189,21 @@ def test_fullsize_gpt_1p3b(dev):
 def test_fullsize_llama7b_16l(dev):
     """3,238,133,760 params, n=4, a=2, ZeRO-2 even, 1% x100 outliers, loss scale 1 (cold start)."""
     run_fullsize(synth.WORKLOADS["llama7b_16l"])
+
+
+def test_fullsize_gpt2_small_single_pass(dev):
+    """The benchmark's workload through dp_step_single_pass, and a skipped step after it."""
+    run_fullsize(synth.WORKLOADS["gpt2_small"], inject=True, single=True)
+
+
+def test_fullsize_gpt_1p3b_single_pass(dev):
+    """The 1.3B list's +3-misaligned 25M-bucket ZeRO-3 layout through the single pass, warm m/v."""
+    run_fullsize(synth.WORKLOADS["gpt_1p3b"], warm=True, single=True)
+
+
+def test_fullsize_llama7b_16l_single_pass(dev):
+    """Llama-16L (3.2B params, heavy-tailed gradients, cold start) through the single pass."""
+    run_fullsize(synth.WORKLOADS["llama7b_16l"], single=True)
 
 
 @pytest.mark.parametrize("psi,n,a,layout", [((1 << 28) + 5, 4, 8, "ragged"), (10 ** 9, 8, 8, "even")])
