@@ -488,10 +488,17 @@ dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, floa
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
 }
 
-dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
-                    const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
-                    float loss_scale, int32_t sum_mode, float* const* gbar_shard, void* ws,
-                    dp_step_state_t* d_state, dp_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// dp_step, optionally preceded by the host-to-device copies of its gradients and followed by the copy of its
+// state to the host (dp_step_from_host).  Every argument is checked before anything is queued.
+dp_status_t step_impl(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                      const uint16_t* const* host_grads, const uint16_t* const* grads, int32_t a,
+                      const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
+                      float* const* gbar_shard, void* ws, dp_step_state_t* d_state, dp_step_state_t* host_state,
+                      cudaStream_t stream) {
   static thread_local Plan P;
   dp_status_t st = build_plan(layout, P);
   if (st != DP_OK) return st;
@@ -501,11 +508,39 @@ dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* cons
     return st;
   if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
   if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  if (host_grads &&
+      (st = check_full_arrays(P, (const void* const*)host_grads, P.n * a, "host_grads")) != DP_OK)
+    return st;
+  const size_t bytes = (size_t)P.psi * sizeof(uint16_t);
+  if (host_grads && bytes) {
+    for (int q = 0; q < P.n * a; ++q) {
+      const cudaError_t e = cudaMemcpyAsync(const_cast<uint16_t*>(grads[q]), host_grads[q], bytes,
+                                            cudaMemcpyHostToDevice, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "gradient copy to the device");
+    }
+  }
   LaunchCount lc;
-  cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, (cudaStream_t)stream, &lc.n);
+  cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
-  e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
-  return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
+  e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, stream, &lc.n);
+  if (e != cudaSuccess) return cuda_fail(e, "update launch");
+  if (host_state) {
+    e = cudaMemcpyAsync(host_state, d_state, sizeof(dp_step_state_t), cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy to the host");
+  }
+  return DP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                    const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                    float loss_scale, int32_t sum_mode, float* const* gbar_shard, void* ws,
+                    dp_step_state_t* d_state, dp_stream_t stream) {
+  return step_impl(replicas, master, m, v, nullptr, grads, a, layout, adam, loss_scale, sum_mode, gbar_shard, ws,
+                   d_state, nullptr, (cudaStream_t)stream);
 }
 
 dp_status_t dp_step_from_host(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
@@ -513,36 +548,9 @@ dp_status_t dp_step_from_host(uint16_t* const* replicas, float* const* master, f
                               const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
                               float* const* gbar_shard, void* ws, dp_step_state_t* d_state,
                               dp_step_state_t* host_state, dp_stream_t stream) {
-  static thread_local Plan P;
-  dp_status_t st = build_plan(layout, P);
-  if (st != DP_OK) return st;
-  StepScalars s;
-  float* gb[DP_MAX_N];
-  // Every argument is checked before anything is queued, as for dp_step.
-  if ((st = prepare_reduce(P, (const uint16_t* const*)grads, a, adam, loss_scale, sum_mode, gbar_shard, ws, d_state,
-                           s, gb)) != DP_OK)
-    return st;
-  if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
-  if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
-  if ((st = check_full_arrays(P, (const void* const*)host_grads, P.n * a, "host_grads")) != DP_OK) return st;
-  const cudaStream_t cs = (cudaStream_t)stream;
-  const size_t bytes = (size_t)P.psi * sizeof(uint16_t);
-  if (bytes) {
-    for (int q = 0; q < P.n * a; ++q) {
-      const cudaError_t e = cudaMemcpyAsync(grads[q], host_grads[q], bytes, cudaMemcpyHostToDevice, cs);
-      if (e != cudaSuccess) return cuda_fail(e, "gradient copy to the device");
-    }
-  }
-  LaunchCount lc;
-  cudaError_t e = launch_pass_a(P, (const uint16_t* const*)grads, a, gb, s, d_state, cs, &lc.n);
-  if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
-  e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, cs, &lc.n);
-  if (e != cudaSuccess) return cuda_fail(e, "update launch");
-  if (host_state) {
-    e = cudaMemcpyAsync(host_state, d_state, sizeof(dp_step_state_t), cudaMemcpyDeviceToHost, cs);
-    if (e != cudaSuccess) return cuda_fail(e, "status copy to the host");
-  }
-  return DP_OK;
+  if (!host_grads) return fail(DP_ERR_INVALID_ARG, "dp_step_from_host: host_grads is NULL");
+  return step_impl(replicas, master, m, v, host_grads, (const uint16_t* const*)grads, a, layout, adam, loss_scale,
+                   sum_mode, gbar_shard, ws, d_state, host_state, (cudaStream_t)stream);
 }
 
 dp_status_t dp_scaler_init(dp_step_state_t* d_state, float scale, dp_stream_t stream) {
