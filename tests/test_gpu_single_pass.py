@@ -38,6 +38,11 @@ CASES = [
     (100_003, 8, 1, 3, "buckets", {"bucket": 23_456, "misalign": 3}),
     (300_007, 5, 3, 2, "random", {"nseg": 200}),
     (65_536, 16, 4, 3, "random", {"nseg": 21}),
+    # shard offsets all multiples of 4 and >= 16 inputs a tile: the variant that keeps gbar in registers and
+    # streams with four stages; shard edges fall inside tiles (12,480 = 7680 + 4800)
+    (7680 * 13, 8, 2, 1, "even", {}),
+    (131_072, 16, 1, 2, "even", {}),
+    (7680 * 40, 4, 8, 3, "even", {}),
 ]
 
 

@@ -35,20 +35,26 @@ constexpr int RA_NPS = 2;                      // inputs per stage: two 15 KB bu
 constexpr int RA_IN_BYTES = TILE * 2;          // one tile of one bf16 input
 constexpr int RA_STAGE_BYTES = RA_NPS * RA_IN_BYTES;
 constexpr int RA_GBAR_FLOATS = TILE + 16;      // single pass: the tile's gbar (+16: last group's overhang)
-// Single pass: + the tile's bf16 staging and its master/m/v (fetched while its gradients stream).
-constexpr int RA_STATE_FLOATS = TILE + 16;
-constexpr int RA_EXTRA_FUSED = RA_GBAR_FLOATS * 4 + TILE * 2 + 3 * RA_STATE_FLOATS * 4;
-// 180 KB of stages in flight; the single pass keeps 90 KB and uses the rest for the tile's gbar, staging and
-// optimizer state.
-template <bool FUSED>
-__host__ __device__ constexpr int ra_stages() { return FUSED ? 3 : 6; }
-template <bool FUSED>
-__host__ __device__ constexpr int ra_bar_offset() { return ra_stages<FUSED>() * RA_STAGE_BYTES + (FUSED ? RA_EXTRA_FUSED : 0); }
+constexpr int RA_STATE_FLOATS = TILE + 16;     // single pass: the tile's old master / m / v, one array each
+// FUSED selects the kernel's job: 0, pass A of the two-pass step (180 KB of stages in flight); 1, the single
+// pass with a shared gbar tile through which the consumer warps regroup gbar into local 4-groups (three
+// stages); 2, the single pass for shards whose offsets are multiples of 4, where each thread's 16 elements
+// already are local 4-groups, so the gbar tile gives way to a fourth stage (chosen with at least 16 inputs a
+// tile).  Both single passes also hold
+// the tile's bf16 staging and its old optimizer state, fetched while its gradients stream.
+template <int FUSED>
+__host__ __device__ constexpr int ra_stages() { return FUSED == 2 ? 4 : FUSED ? 3 : 6; }
+template <int FUSED>
+__host__ __device__ constexpr int ra_gbar_bytes() { return FUSED == 1 ? RA_GBAR_FLOATS * 4 : 0; }
+template <int FUSED>
+__host__ __device__ constexpr int ra_extra() { return FUSED ? ra_gbar_bytes<FUSED>() + TILE * 2 + 3 * RA_STATE_FLOATS * 4 : 0; }
+template <int FUSED>
+__host__ __device__ constexpr int ra_bar_offset() { return ra_stages<FUSED>() * RA_STAGE_BYTES + ra_extra<FUSED>(); }
 // Barriers: full/empty per stage, the single pass's state full/empty, abort, count.
-template <bool FUSED>
+template <int FUSED>
 __host__ __device__ constexpr int ra_smem() { return ra_bar_offset<FUSED>() + 2 * ra_stages<FUSED>() * 8 + (FUSED ? 16 : 0) + 32; }
-static_assert(ra_smem<true>() + 64 <= 227 * 1024, "single-pass shared memory fits one CTA");
-static_assert(ra_smem<false>() + 64 <= 227 * 1024, "shared memory fits one CTA");
+static_assert(ra_smem<0>() + 64 <= 227 * 1024 && ra_smem<1>() + 64 <= 227 * 1024 && ra_smem<2>() + 64 <= 227 * 1024,
+              "shared memory fits one CTA");
 static_assert(TILE == RA_CTHREADS * RA_EPT, "one 16-element group per consumer thread");
 static_assert(RA_IN_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
 
@@ -167,6 +173,51 @@ __device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, cons
   }
 }
 
+// Single pass, gbar in registers (FUSED 2): one local element j of tile t -- Adam with gbar g on the old
+// state (shared memory inside the tile's 4-aligned local interior [jlo, jhi), the current set at its ragged
+// ends), the new state into the other set, the bf16 image into the staging tile at the element's global
+// position in the cell.
+struct SpTile {
+  int64_t delta, cb, jlo, jhi;
+  int cur, owner;
+};
+template <int MAXSEG>
+__device__ __forceinline__ void sp_update1(const ReduceParams<MAXSEG>& p, const SpTile& T, const AdamK& K, float g,
+                                           int64_t j, const float* s_state, uint16_t* s_stage) {
+  float th, mm, vv;
+  if (j >= T.jlo && j < T.jhi) {
+    th = s_state[j - T.jlo];
+    mm = s_state[RA_STATE_FLOATS + (j - T.jlo)];
+    vv = s_state[2 * RA_STATE_FLOATS + (j - T.jlo)];
+  } else {
+    th = p.st_master[T.cur][T.owner][j];
+    mm = p.st_m[T.cur][T.owner][j];
+    vv = p.st_v[T.cur][T.owner][j];
+  }
+  adam1(g, th, mm, vv, K);
+  p.st_master[T.cur ^ 1][T.owner][j] = th;
+  p.st_m[T.cur ^ 1][T.owner][j] = mm;
+  p.st_v[T.cur ^ 1][T.owner][j] = vv;
+  s_stage[j - T.delta - T.cb] = bf16_rn(th);
+}
+// Four local elements [j, j + 4), j a multiple of 4 inside [jlo, jhi): 16-byte accesses.
+template <int MAXSEG>
+__device__ __forceinline__ void sp_update4(const ReduceParams<MAXSEG>& p, const SpTile& T, const AdamK& K, float g0,
+                                           float g1, float g2, float g3, int64_t j, const float* s_state,
+                                           uint16_t* s_stage) {
+  float4 th = *reinterpret_cast<const float4*>(s_state + (j - T.jlo));
+  float4 mm = *reinterpret_cast<const float4*>(s_state + RA_STATE_FLOATS + (j - T.jlo));
+  float4 vv = *reinterpret_cast<const float4*>(s_state + 2 * RA_STATE_FLOATS + (j - T.jlo));
+  adam1(g0, th.x, mm.x, vv.x, K);
+  adam1(g1, th.y, mm.y, vv.y, K);
+  adam1(g2, th.z, mm.z, vv.z, K);
+  adam1(g3, th.w, mm.w, vv.w, K);
+  *reinterpret_cast<float4*>(p.st_master[T.cur ^ 1][T.owner] + j) = th;
+  *reinterpret_cast<float4*>(p.st_m[T.cur ^ 1][T.owner] + j) = mm;
+  *reinterpret_cast<float4*>(p.st_v[T.cur ^ 1][T.owner] + j) = vv;
+  stage_bf16x4(s_stage, j - T.delta - T.cb, bf16x2_rn(th.x, th.y), bf16x2_rn(th.z, th.w));
+}
+
 // Fold input HH of a stage (8 words = 16 bf16 of this thread) into the accumulators, ring order.
 //  compensated: one (H, L) pair through the whole sequence, (H, e) = TwoSum(H, x), L = L + e (first: H = x);
 //  plain: each rank's micro-steps summed left to right in h (kfirst starts a rank), and at the rank's last
@@ -193,15 +244,16 @@ __device__ __forceinline__ void fold_input(f2_t (&H)[8], f2_t (&L)[8], f2_t (&h)
   }
 }
 
-template <int MAXSEG, bool COMP, bool FUSED>
+template <int MAXSEG, bool COMP, int FUSED>
 __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceParams<MAXSEG> p) {
   constexpr int NST = ra_stages<FUSED>();
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
+  // single pass: the gbar tile (FUSED 1), the bf16 staging tile (global position in the cell), the tile's old
+  // master, m, v (4-aligned local interior), RA_STATE_FLOATS apart
   float* s_g = reinterpret_cast<float*>(smem + NST * RA_STAGE_BYTES);
-  uint16_t* s_stage = reinterpret_cast<uint16_t*>(smem + NST * RA_STAGE_BYTES + RA_GBAR_FLOATS * 4);
-  // single pass: the tile's master, m, v (4-aligned local interior), RA_STATE_FLOATS apart
-  float* s_state = reinterpret_cast<float*>(smem + NST * RA_STAGE_BYTES + RA_GBAR_FLOATS * 4 + TILE * 2);
+  uint16_t* s_stage = reinterpret_cast<uint16_t*>(smem + NST * RA_STAGE_BYTES + ra_gbar_bytes<FUSED>());
+  float* s_state = reinterpret_cast<float*>(smem + NST * RA_STAGE_BYTES + ra_gbar_bytes<FUSED>() + TILE * 2);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ra_bar_offset<FUSED>());
   uint64_t* empty = full + NST;
   uint64_t* sfull = empty + NST;        // single pass: the tile's state has landed (producer + bytes)
@@ -447,17 +499,22 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
         for (int u = 0; u < RA_EPT; ++u)
           if ((whole || (e0 + u >= t.start && e0 + u < t.end)) && nonfinite(o[u])) ++bad;
       }
-      if constexpr (FUSED) {
-        // Single pass: hand the tile's gbar to its update through shared memory (indexed by global position).
+      if constexpr (FUSED != 0) {
         const int64_t cb = (t.start / TILE) * TILE;
-        named_bar_sync(1, RA_CTHREADS);    // the previous tile's update is done with s_g and s_stage
-        if (tid == 0) bulk_wait_read<0>(); // and its replica stores have read s_stage
-        if (active) {
-          float4* gp = reinterpret_cast<float4*>(s_g + (e0 - cb));
+        if constexpr (FUSED == 1) {
+          // Hand the tile's gbar to its update through shared memory (indexed by global position).
+          named_bar_sync(1, RA_CTHREADS);    // the previous tile's update is done with s_g and s_stage
+          if (tid == 0) bulk_wait_read<0>(); // and its replica stores have read s_stage
+          if (active) {
+            float4* gp = reinterpret_cast<float4*>(s_g + (e0 - cb));
 #pragma unroll
-          for (int u = 0; u < RA_EPT; u += 4) gp[u / 4] = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+            for (int u = 0; u < RA_EPT; u += 4) gp[u / 4] = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+          }
+          named_bar_sync(1, RA_CTHREADS);
+        } else {
+          if (tid == 0) bulk_wait_read<0>(); // the previous tile's replica stores have read s_stage
+          named_bar_sync(1, RA_CTHREADS);
         }
-        named_bar_sync(1, RA_CTHREADS);
         AdamK K;
         K.b1 = p.b1f; K.b2 = p.b2f; K.omb1 = p.omb1; K.omb2 = p.omb2; K.eps = p.eps;
         K.step = s_k[0];
@@ -468,7 +525,30 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
           *s_abort = 1;
           live = false;
         }
-        fused_update(p, t, K, s_cur, s_g, s_stage, s_state, tid);
+        if constexpr (FUSED == 1) {
+          fused_update(p, t, K, s_cur, s_g, s_stage, s_state, tid);
+        } else {
+          // Every thread updates the elements whose gbar it holds: with every shard offset a multiple of 4 (the
+          // launcher's condition for this variant) a thread's 16 elements are four aligned 4-groups in local
+          // space too; a group at a segment edge is updated element by element.
+          SpTile T;
+          T.delta = t.loff - t.goff;
+          T.cb = cb;
+          T.jlo = (t.start + T.delta + 3) & ~int64_t(3);
+          T.jhi = (t.end + T.delta) & ~int64_t(3);
+          T.cur = s_cur;
+          T.owner = t.owner;
+          const int64_t Lt = e0 + T.delta;
+          if (whole && (Lt & 3) == 0) {
+#pragma unroll
+            for (int u = 0; u < RA_EPT; u += 4)
+              sp_update4(p, T, K, o[u], o[u + 1], o[u + 2], o[u + 3], Lt + u, s_state, s_stage);
+          } else if (active) {
+#pragma unroll
+            for (int u = 0; u < RA_EPT; ++u)
+              if (e0 + u >= t.start && e0 + u < t.end) sp_update1(p, T, K, o[u], Lt + u, s_state, s_stage);
+          }
+        }
         // Order this thread's reads of s_state (and writes of s_stage) before the async proxy's next use of
         // them, then hand s_state back to the producer.
         fence_proxy_async_smem();
@@ -901,7 +981,7 @@ struct FusedArgs {
   uint16_t* const* rep;  // n
 };
 
-template <int MAXSEG, bool COMP, bool FUSED>
+template <int MAXSEG, bool COMP, int FUSED>
 static cudaError_t launch_reduce_t(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
                                    const StepScalars& s, int advance, dp_step_state_t* st, const FusedArgs* fa,
                                    cudaStream_t stream) {
@@ -958,10 +1038,10 @@ cudaError_t launch_reduce(const Plan& P, const uint16_t* const* g, int a, float*
   ++*launches;
   const bool comp = s.mode == DP_SUM_COMPENSATED;
   if (P.nseg <= SMALL_SEG)
-    return comp ? launch_reduce_t<SMALL_SEG, true, false>(P, g, a, gbar, s, advance, st, nullptr, stream)
-                : launch_reduce_t<SMALL_SEG, false, false>(P, g, a, gbar, s, advance, st, nullptr, stream);
-  return comp ? launch_reduce_t<BIG_SEG, true, false>(P, g, a, gbar, s, advance, st, nullptr, stream)
-              : launch_reduce_t<BIG_SEG, false, false>(P, g, a, gbar, s, advance, st, nullptr, stream);
+    return comp ? launch_reduce_t<SMALL_SEG, true, 0>(P, g, a, gbar, s, advance, st, nullptr, stream)
+                : launch_reduce_t<SMALL_SEG, false, 0>(P, g, a, gbar, s, advance, st, nullptr, stream);
+  return comp ? launch_reduce_t<BIG_SEG, true, 0>(P, g, a, gbar, s, advance, st, nullptr, stream)
+              : launch_reduce_t<BIG_SEG, false, 0>(P, g, a, gbar, s, advance, st, nullptr, stream);
 }
 
 // After a single-pass step: if it was skipped, rewrite the replicas as bf16 of the current (unchanged) master.
@@ -992,9 +1072,16 @@ __global__ void __launch_bounds__(256) repair_kernel(const __grid_constant__ Rep
 template <int MAXSEG>
 static cudaError_t launch_single_t(const Plan& P, const uint16_t* const* g, int a, const StepScalars& s,
                                    dp_step_state_t* st, const FusedArgs& fa, cudaStream_t stream) {
-  cudaError_t e = s.mode == DP_SUM_COMPENSATED
-                      ? launch_reduce_t<MAXSEG, true, true>(P, g, a, nullptr, s, 1, st, &fa, stream)
-                      : launch_reduce_t<MAXSEG, false, true>(P, g, a, nullptr, s, 1, st, &fa, stream);
+  // gbar stays in registers when every shard offset keeps 4-groups aligned and a tile has enough inputs for the
+  // fourth stage to pay; otherwise the shared gbar tile regroups it.
+  bool realign = P.n * a >= 16;
+  for (int k = 0; k < P.nseg; ++k)
+    if (((P.e[k].loff - P.e[k].goff) & 3) != 0) realign = false;
+  const bool comp = s.mode == DP_SUM_COMPENSATED;
+  cudaError_t e = realign ? (comp ? launch_reduce_t<MAXSEG, true, 2>(P, g, a, nullptr, s, 1, st, &fa, stream)
+                                  : launch_reduce_t<MAXSEG, false, 2>(P, g, a, nullptr, s, 1, st, &fa, stream))
+                          : (comp ? launch_reduce_t<MAXSEG, true, 1>(P, g, a, nullptr, s, 1, st, &fa, stream)
+                                  : launch_reduce_t<MAXSEG, false, 1>(P, g, a, nullptr, s, 1, st, &fa, stream));
   if (e != cudaSuccess) return e;
   RepairParams<MAXSEG> rp;
   for (int r = 0; r < P.n; ++r) {
