@@ -94,7 +94,7 @@ struct StagePos {
 };
 
 // Fold input HH of a stage (4 words = 8 bf16 of this thread) into rank r's partial sum `cur` (kfirst: its first
-// micro-step; compensated: Fast2Sum with the error terms in cur.l).  At the rank's last micro-step (klast) the
+// micro-step; compensated: Knuth TwoSum with the error terms in cur.l).  At the rank's last micro-step (klast) the
 // rank is complete: the slots below the lowest clear bit of r are all occupied and merge into it, and that
 // bit's slot takes the sum (static slot indices keep every slot in registers).  When r completes a block of
 // 2^LEVELS ranks, cur is left holding the total.
@@ -109,7 +109,7 @@ __device__ __forceinline__ void tree_fold(Part8 (&slot)[LEVELS], Part8& cur, con
       cur.l[u] = 0ull;
     } else if (COMP) {
       f2_t e;
-      cur.h[u] = f2_fast_two_sum(cur.h[u], xx, e);
+      cur.h[u] = f2_two_sum(cur.h[u], xx, e);
       cur.l[u] = f2_add(cur.l[u], e);
     } else {
       cur.h[u] = f2_add(cur.h[u], xx);
