@@ -623,9 +623,12 @@ def _fs_type(path: str) -> str:
 def main():
     args = parse()
     import synth
-    if args.workload not in synth.WORKLOADS:
-        raise SystemExit("unknown workload %s (have %s)" % (args.workload, ", ".join(synth.WORKLOADS)))
-    wl = synth.WORKLOADS[args.workload]
+    known = dict(synth.WORKLOADS)
+    known.update({w.name: w for w in synth.sweep_cases()})   # the flat sweep's cases, e.g. sweep_1000000000_n8_a8_even
+    if args.workload not in known:
+        raise SystemExit("unknown workload %s (have %s, and the sweep_* cases)" %
+                         (args.workload, ", ".join(synth.WORKLOADS)))
+    wl = known[args.workload]
     if args.psi > 0:
         wl = wl.with_(psi=args.psi, description=wl.description + " [psi overridden to %d]" % args.psi)
     if args.impl == "reference":
