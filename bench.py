@@ -7,6 +7,11 @@ reduced in ring order, averaged, unscaled and finite-checked, partitioned Adam o
 all-gather into the n replicas (dp_step_reduce + dp_step_update, the two kernels of dp_step).  The default
 workload is the GPT-2-small parameter list (123,568,896 params), n=8, a=4, ZeRO-1 even shards, loss scale 2^16.
 
+The end-to-end leg ("e2e") times dp_step_from_host: every step's gradients copied from pinned host memory, the
+step, and the 64-byte step state read back, in one C-ABI call.  --path single-pass / microstep time
+dp_step_single_pass or the per-micro-step reduce-scatter instead; --order tree the binomial-tree order;
+--workload also takes the flat sweep's case names (sweep_<psi>_n<n>_a<a>_<even|ragged>).
+
 Multi-GPU (torchrun): the path does not shard across GPUs; every rank runs an independent replica of the
 workload (weak scaling), with a barrier and max-over-ranks timing and no collective in the data path.
 
