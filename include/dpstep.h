@@ -167,15 +167,21 @@ typedef struct {
 
 /* ---- host helpers (no GPU needed) --------------------------------------- */
 
+/* Version of this ABI (not on the pages). */
 int32_t dp_abi_version(void);
 
-/* Name of a status code. */
+/* Name of a status code (not on the pages). */
 const char* dp_status_str(dp_status_t s);
 
-/* Message of the last failing call on this host thread ("" if none). */
+/* Message of the last failing call on this host thread ("" if none; not on the pages). */
 const char* dp_last_error(void);
 
-/* Checks a layout against the rules of dp_layout_t.  DP_OK or DP_ERR_INVALID_ARG. */
+/* Checks a layout against the rules of dp_layout_t.  DP_OK or DP_ERR_INVALID_ARG.
+ * The shard layout follows "Distributed Training: Split along the Four Axes",
+ * ZeRO/FSDP paragraph (each rank keeps only its shard of the optimizer state)
+ * and "Data vs Tensor vs Pipeline Parallelism", "FSDP wrapping granularity"
+ * (shards per wrapped unit); the pages fix no layout rule, these are the
+ * library's. */
 dp_status_t dp_layout_validate(const dp_layout_t* layout);
 
 /* Builds the standard layouts.  bucket <= 0: one bucket of psi elements.
@@ -187,16 +193,19 @@ dp_status_t dp_layout_validate(const dp_layout_t* layout);
 dp_status_t dp_layout_even(int64_t psi, int32_t n, int64_t bucket, int32_t misalign, dp_segment_t* out,
                            int32_t* nseg);
 
-/* Local length of rank's shard arrays (end of its furthest segment); -1 on error. */
+/* Local length of rank's shard arrays (end of its furthest segment); -1 on
+ * error.  Not on the pages: a size query of the layout above. */
 int64_t dp_shard_len(const dp_layout_t* layout, int32_t rank);
 
 /* Bytes of device workspace that dp_step needs when the caller passes ws
  * instead of gbar_shard pointers: the n averaged-gradient shards, each
- * 256-byte aligned.  0 on error. */
+ * 256-byte aligned.  0 on error.  The shards are the reduce-scatter's output
+ * ("Distributed Training: Split along the Four Axes", ZeRO/FSDP paragraph:
+ * the reduce-scatter leaves each rank only its own shard of the gradient). */
 size_t dp_workspace_size(const dp_layout_t* layout);
 
 /* Floats per rank in a dp_accumulate accumulator: psi (plain) or 2 psi
- * (compensated, interleaved hi, lo). */
+ * (compensated, interleaved hi, lo).  Not on the pages: a size query. */
 size_t dp_acc_elems(int64_t psi, int32_t sum_mode);
 
 /* B_global = b x n x a: tensor and pipeline degrees are not multiplied in
@@ -220,18 +229,19 @@ dp_status_t dp_memory_model(int32_t stage, int64_t psi, int32_t n, double out[4]
 dp_status_t dp_traffic_model(int32_t stage, int64_t psi, int32_t n, int32_t wire_bytes_grad,
                              int32_t wire_bytes_param, double out[3]);
 
-/* Upper bound, in nanoseconds, of every device-side wait of the kernels
+/* Not on the pages: upper bound, in nanoseconds, of every device-side wait of the kernels
  * (default 2 s).  A wait that runs out records DP_ERR_TIMEOUT in
  * state.error and the kernel returns; the step is skipped. */
 void dp_set_wait_timeout_ns(uint64_t ns);
 uint64_t dp_get_wait_timeout_ns(void);
 
-/* Number of kernels this library has launched in this process. */
+/* Number of kernels this library has launched in this process (not on the pages). */
 uint64_t dp_kernel_launches(void);
 
 /* ---- device entry points -------------------------------------------------- */
 
-/* Sets *d_state to t = 0, beta powers 1, no skip, no error (one kernel). */
+/* Sets *d_state to t = 0, beta powers 1, no skip, no error (one kernel).
+ * Not on the pages: initialisation of the library's step state. */
 dp_status_t dp_state_init(dp_step_state_t* d_state, dp_stream_t stream);
 
 /* Staged accumulation of one micro-step (data-parallel paragraphs: each rank
@@ -243,8 +253,12 @@ dp_status_t dp_state_init(dp_step_state_t* d_state, dp_stream_t stream);
 dp_status_t dp_accumulate(float* const* acc, const uint16_t* const* g, int64_t psi, int32_t n, int32_t first,
                           int32_t sum_mode, dp_stream_t stream);
 
-/* Staged reduce-scatter + average + unscale + non-finite check.  For each
- * segment (owner s) and element i in it:
+/* Staged reduce-scatter + average + unscale + non-finite check ("Data vs
+ * Tensor vs Pipeline Parallelism", "Data parallelism: split the batch": the
+ * ring all-reduce is a reduce-scatter then an all-gather, and sharded data
+ * parallelism keeps only the reduce-scatter's shard; "Distributed Training:
+ * Split along the Four Axes", data-parallel averaging paragraph: gbar =
+ * sum_r g_r / n).  For each segment (owner s) and element i in it:
  *   p = acc_{s+1} + acc_{s+2} + ... + acc_s   (ring order: the chunk starts at
  *       rank s+1 and reaches its owner after n-1 hops; compensated mode adds
  *       (hi, lo) pairs with TwoSum and ends with hi + lo; with DP_ORDER_TREE
@@ -285,7 +299,12 @@ dp_status_t dp_reduce_scatter_micro(float* const* acc_shard, float* const* gbar_
                                     dp_adam_t adam, float loss_scale, int32_t sum_mode, dp_step_state_t* d_state,
                                     dp_stream_t stream);
 
-/* Staged partitioned Adam.  Unless state.found_inf: t += 1, beta powers
+/* Staged partitioned Adam ("Distributed Training: Split along the Four
+ * Axes", memory-budget paragraph: an fp32 master copy and Adam's two moments
+ * per parameter; ZeRO/FSDP paragraph: each rank updates only its shard, and
+ * sharding does not change the update).  The Adam equations themselves are
+ * not on the pages (standard Adam, see the file comment).
+ * Unless state.found_inf: t += 1, beta powers
  * advance, then for every element of every shard (stage 0: of every rank's
  * full arrays, with the owner's gbar):
  *   m = b1 m + (1-b1) g ; v = b2 v + (1-b2) g^2 ;
@@ -295,12 +314,20 @@ dp_status_t dp_reduce_scatter_micro(float* const* acc_shard, float* const* gbar_
 dp_status_t dp_adam_shard(float* const* master, float* const* m, float* const* v, const float* const* gbar_shard,
                           const dp_layout_t* layout, dp_adam_t adam, dp_step_state_t* d_state, dp_stream_t stream);
 
-/* Staged all-gather: unless state.found_inf, replicas[r][i] = bf16_rne(theta_i)
+/* Staged all-gather ("Distributed Training: Split along the Four Axes",
+ * ZeRO/FSDP paragraph: the updated parameter shards are all-gathered so every
+ * rank again holds the whole model; data-parallel paragraph: the replicas stay
+ * identical): unless state.found_inf, replicas[r][i] = bf16_rne(theta_i)
  * for every rank r (stage 0: rank r's own master).  replicas[r]: device, psi bf16. */
 dp_status_t dp_allgather_params(uint16_t* const* replicas, const float* const* master, const dp_layout_t* layout,
                                 const dp_step_state_t* d_state, dp_stream_t stream);
 
 /* The fused step: dp_step_reduce then dp_step_update (two kernels).
+ * It is the whole data-parallel step of "Distributed Training: Split along the
+ * Four Axes" (data-parallel paragraphs: accumulate a micro-steps, one
+ * all-reduce, gbar = sum / n; ZeRO/FSDP paragraph: sharded optimizer state)
+ * with the ring of "Data vs Tensor vs Pipeline Parallelism", "Data
+ * parallelism: split the batch".
  * grads: host array of n*a device pointers, rank-major (grads[r*a + k] is
  * micro-step k of rank r), each psi bf16.  Per element the gradient is summed
  * in a fixed order -- ranks in ring order s+1, ..., s for the owner s, each
@@ -319,7 +346,8 @@ dp_status_t dp_step(uint16_t* const* replicas, float* const* master, float* cons
                     float loss_scale, int32_t sum_mode, float* const* gbar_shard, void* ws,
                     dp_step_state_t* d_state, dp_stream_t stream);
 
-/* dp_step with the step's gradients in host memory: the end-to-end call of a
+/* dp_step with the step's gradients in host memory (same passages as dp_step;
+ * the copies are not on the pages): the end-to-end call of a
  * loop whose gradients arrive on the host.  On `stream`, in order: the n*a
  * host buffers host_grads[q] (psi bf16 each, rank-major like grads) are
  * copied into the caller's device buffers grads[q] (one cudaMemcpyAsync
@@ -337,7 +365,8 @@ dp_status_t dp_step_from_host(uint16_t* const* replicas, float* const* master, f
                               float* const* gbar_shard, void* ws, dp_step_state_t* d_state,
                               dp_step_state_t* host_state, dp_stream_t stream);
 
-/* First half of dp_step (one kernel): accumulate + ring reduce-scatter +
+/* First half of dp_step (one kernel; same passages as dp_step):
+ * accumulate + ring reduce-scatter +
  * average + unscale + non-finite check, gbar into the shards; the last CTA
  * publishes found_inf / nonfinite and, unless found, advances t and the
  * beta powers for the update that follows. */
@@ -345,7 +374,8 @@ dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* c
                            const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
                            dp_step_state_t* d_state, dp_stream_t stream);
 
-/* Second half of dp_step (one kernel): unless found_inf, Adam on every shard
+/* Second half of dp_step (one kernel; same passages as dp_adam_shard and
+ * dp_allgather_params): unless found_inf, Adam on every shard
  * and the bf16 all-gather into every replica, reading the gbar shards and the
  * beta powers dp_step_reduce left. */
 dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
@@ -353,10 +383,15 @@ dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, floa
                            const dp_step_state_t* d_state, dp_stream_t stream);
 
 /* Sets the device-resident dynamic loss scale of *d_state to `scale` (> 0,
- * finite) and good_steps to 0 (one kernel).  Other fields are untouched. */
+ * finite) and good_steps to 0 (one kernel).  Other fields are untouched.
+ * ("Distributed Training: Split along the Four Axes", checkpoint and
+ * evaluation paragraphs name the loss scale as training state.) */
 dp_status_t dp_scaler_init(dp_step_state_t* d_state, float scale, dp_stream_t stream);
 
-/* dp_step with a dynamic loss scale: the reduction unscales by the scale held
+/* dp_step with a dynamic loss scale ("Distributed Training: Split along the
+ * Four Axes", checkpoint and evaluation paragraphs: the loss scale is state
+ * to keep and align; the growth/back-off rule is not on the pages, see
+ * dp_scaler_t): the reduction unscales by the scale held
  * in d_state->loss_scale (read on the device, so no host round trip), and the
  * last CTA of the reduction updates that scale with `scaler` once the skip
  * decision is known.  A scale that is not positive and finite, or whose
@@ -367,7 +402,9 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
                            const dp_scaler_t* scaler, int32_t sum_mode, float* const* gbar_shard, void* ws,
                            dp_step_state_t* d_state, dp_stream_t stream);
 
-/* The fused step in ONE pass over memory (one reduce-and-update kernel, plus a
+/* The fused step in ONE pass over memory (same passages as dp_step; the
+ * skip rule of the file comment kept by double-buffering the state, which the
+ * pages do not describe) (one reduce-and-update kernel, plus a
  * repair kernel that does work only on a skipped step).  The optimizer state
  * is double-buffered: master, m and v are host arrays of 2n device pointers,
  * set 0 (entries 0..n-1) and set 1 (entries n..2n-1), each like dp_step's.
@@ -386,10 +423,12 @@ dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master,
                                 float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream);
 
 /* Reads found_inf and error of *d_state into host ints after synchronising
- * the stream (the one blocking call).  skipped / err may be NULL. */
+ * the stream (the one blocking call).  skipped / err may be NULL.  Not on the
+ * pages: a host-side read of the step's device-resident status. */
 dp_status_t dp_read_status(const dp_step_state_t* d_state, int32_t* skipped, int32_t* err, dp_stream_t stream);
 
-/* Self-test of the bounded wait: launches one block that waits on a barrier
+/* Self-test of the bounded wait (not on the pages; the failure handling of
+ * every device wait): launches one block that waits on a barrier
  * nothing will complete; after timeout_ns it records DP_ERR_TIMEOUT in
  * d_state->error and returns, leaving the context usable. */
 dp_status_t dp_selftest_wait_timeout(dp_step_state_t* d_state, uint64_t timeout_ns, dp_stream_t stream);
@@ -409,11 +448,12 @@ dp_status_t dp_selftest_wait_timeout(dp_step_state_t* d_state, uint64_t timeout_
  * until the process exits): the layout's dp_workspace_size must not exceed
  * it (about 16 million parameters), else DP_ERR_INVALID_ARG and nothing is
  * launched.  Arguments, results and errors are those of dp_step; no call
- * allocates or frees memory.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) -- make it before any stream
- * capture on that device.  All calls share the array and it keeps the last
- * call's contents; calls whose kernels overlap on the GPU race on it, so
- * order them (one stream, or events). */
+ * allocates or frees memory.  Every call looks up the array's device address
+ * in the current context (cudaGetSymbolAddress; the first call on a device
+ * also loads the library's kernels there) -- make the first call on a device
+ * before any stream capture on that device.  All calls share the array and it
+ * keeps the last call's contents; calls whose kernels overlap on the GPU race
+ * on it, so order them (one stream, or events). */
 dp_status_t dp_step_static(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
                            const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
                            float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream);
@@ -460,7 +500,9 @@ dp_status_t dp_checkpoint_save(const char* root, const char* tag, const dp_layou
                                const dp_step_state_t* d_state, const void* user_meta, uint64_t user_meta_bytes,
                                int32_t host_buffers, dp_stream_t stream);
 
-/* Loads the checkpoint `tag` (NULL: the one LATEST names) into `layout`,
+/* Loads the checkpoint `tag` (NULL: the one LATEST names) into `layout`
+ * (same passages as dp_checkpoint_save: a restart reshards to the new world
+ * size or refuses),
  * which must have the saved psi and may differ in everything else.  Every
  * element lands at its global position's place in the new layout, so the
  * result is a bit-exact permutation of what was saved.  verify = 1 checks
@@ -475,7 +517,8 @@ dp_status_t dp_checkpoint_load(const char* root, const char* tag, const dp_layou
                                void* user_meta, uint64_t* user_meta_bytes, int32_t host_buffers, int32_t verify,
                                dp_stream_t stream);
 
-/* The saved layout of checkpoint `tag` (NULL: LATEST) and the size of its
+/* The saved layout of checkpoint `tag` (NULL: LATEST; same passages as
+ * dp_checkpoint_save: the parallel layout is saved with the state) and the size of its
  * user bytes: any output may be NULL; seg receives the nseg segments if
  * seg_cap is large enough (else DP_ERR_INVALID_ARG).  verify as for
  * dp_checkpoint_load.  Reads no shard data unless verify is set. */

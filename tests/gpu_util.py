@@ -56,8 +56,8 @@ def make_case(wl: synth.Workload, stage: Optional[int] = None, segs=None, t: int
     return Case(wl, segs, stage, dp.Layout(stage, wl.n, wl.psi, segs), grads, master, m, v, t)
 
 
-def upload(c: Case, device="cuda", second_set: bool = False) -> StepBuffers:
-    b = StepBuffers(c.layout, c.wl.a, device, second_set=second_set)
+def upload(c: Case, device="cuda", second_set: bool = False, micro_acc: bool = False) -> StepBuffers:
+    b = StepBuffers(c.layout, c.wl.a, device, second_set=second_set, micro_acc=micro_acc)
     for q, g in enumerate(c.grads):
         b.grads[q].copy_(sd.bf16_from_bits(g))
     sd.place_full(b.master, c.master, c.segs, c.stage)
@@ -68,6 +68,37 @@ def upload(c: Case, device="cuda", second_set: bool = False) -> StepBuffers:
     if c.t:
         b.state.copy_(torch.frombuffer(bytearray(state_bytes(c.t, c.wl.beta1, c.wl.beta2)), dtype=torch.uint8))
     return b
+
+
+BAND = 256         # sentinel bytes on each side of a guarded buffer
+SENTINEL = 0xA5
+
+
+class Guarded:
+    """Moves every device buffer of a StepBuffers into an allocation with BAND sentinel bytes before and after
+    it (content kept), so that a kernel store outside any buffer lands in a band; check() finds it.  The
+    interiors start BAND bytes into their allocation, so base pointers keep 256-byte alignment."""
+
+    NAMES = ("grads", "replicas", "master", "m", "v", "gbar", "master1", "m1", "v1", "acc")
+
+    def __init__(self, b: StepBuffers):
+        self.outer = []
+        for name in self.NAMES:
+            setattr(b, name, [self._wrap(t) for t in getattr(b, name)])
+        b.state = self._wrap(b.state)
+
+    def _wrap(self, t: torch.Tensor) -> torch.Tensor:
+        nb = t.numel() * t.element_size()
+        o = torch.full((2 * BAND + nb,), SENTINEL, dtype=torch.uint8, device=t.device)
+        inner = o[BAND:BAND + nb].view(t.dtype)
+        inner.copy_(t)
+        self.outer.append((o, nb))
+        return inner
+
+    def check(self, what: str = "") -> None:
+        bands = torch.cat([x for o, nb in self.outer for x in (o[:BAND], o[BAND + nb:])])
+        bad = int((bands != SENTINEL).sum().item())
+        assert bad == 0, "%s: %d sentinel bytes overwritten outside the buffers" % (what, bad)
 
 
 def run_oracle(c: Case, threads: int = 8):
@@ -156,3 +187,59 @@ def snapshot(b: StepBuffers) -> List[bytes]:
     torch.cuda.synchronize()
     ts = b.master + b.m + b.v + b.replicas
     return [t.detach().cpu().view(torch.uint8).numpy().tobytes() for t in ts]
+
+
+# ------------------------------------------------------------------ full-size runs checked on sampled elements
+
+def sample_indices(wl, segs, count, seed):
+    rng = np.random.default_rng(seed)
+    idx = set(rng.integers(0, wl.psi, count).tolist())
+    for g, ln, o, lo in segs:
+        if ln:
+            idx.update([g, g + ln - 1, min(g + 1, g + ln - 1), max(g, g + ln - 2)])
+    idx.update(range(max(0, wl.psi - 9), wl.psi))
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+def owners_of(segs, idx):
+    """Owner rank and local index of each global index."""
+    goff = np.array([s[0] for s in segs if s[1]], dtype=np.int64)
+    own = np.array([s[2] for s in segs if s[1]], dtype=np.int64)
+    loff = np.array([s[3] for s in segs if s[1]], dtype=np.int64)
+    k = np.searchsorted(goff, idx, side="right") - 1
+    return own[k], loff[k] + (idx - goff[k])
+
+
+def gather_state(arrs, segs, idx, stage):
+    """Values of per-rank state arrays at global indices (rank 0's copy for plain data parallelism)."""
+    if stage == 0:
+        return arrs[0][torch.from_numpy(idx).to(arrs[0].device)].cpu().numpy()
+    own, loc = owners_of(segs, idx)
+    out = np.zeros(idx.size, np.float32)
+    for r in np.unique(own):
+        sel = np.nonzero(own == r)[0]
+        t = torch.from_numpy(loc[sel]).to(arrs[int(r)].device)
+        out[sel] = arrs[int(r)][t].cpu().numpy()
+    return out
+
+
+def oracle_at(wl, idx, t0=0, m=None, v=None, master=None, prior=False):
+    """The oracle's step on the sampled elements only (the step is elementwise; found is per element)."""
+    ns = idx.size
+    contiguous = ns > 0 and idx[-1] - idx[0] == ns - 1
+    if contiguous:   # a chunk of the space: the generator's contiguous path gives the same values, faster
+        grads = [synth.grads_bf16(wl, r, k, int(idx[0]), ns, prior=prior) for r in range(wl.n) for k in range(wl.a)]
+    else:
+        grads = [synth.grads_bf16_at(wl, r, k, idx, prior=prior) for r in range(wl.n) for k in range(wl.a)]
+    if master is None:
+        master = synth.master_f32(wl, int(idx[0]), ns) if contiguous else synth.master_f32_at(wl, idx)
+    M = [master.copy()]
+    Mm = [m.copy() if m is not None else np.zeros(ns, np.float32)]
+    Vv = [v.copy() if v is not None else np.zeros(ns, np.float32)]
+    M += [np.zeros(0, np.float32)] * (wl.n - 1)
+    Mm += [np.zeros(0, np.float32)] * (wl.n - 1)
+    Vv += [np.zeros(0, np.float32)] * (wl.n - 1)
+    reps = [np.zeros(ns, np.uint16) for _ in range(wl.n)]
+    res = oracle.step(ns, wl.n, wl.a, 1, [(0, ns, 0, 0)], grads, M, Mm, Vv, reps, wl.lr, wl.beta1, wl.beta2,
+                      wl.eps, wl.loss_scale, t0, threads=16)
+    return {"master": M[0], "m": Mm[0], "v": Vv[0], "replicas": reps, **res}

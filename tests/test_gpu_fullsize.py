@@ -13,7 +13,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import synth
 import zero_gradient_sync_gb300 as dp
 from synth import device as sd
@@ -26,67 +25,13 @@ pytestmark = pytest.mark.gpu
 CHUNK = 1 << 26
 
 
-def sample_indices(wl, segs, count, seed):
-    rng = np.random.default_rng(seed)
-    idx = set(rng.integers(0, wl.psi, count).tolist())
-    for g, ln, o, lo in segs:
-        if ln:
-            idx.update([g, g + ln - 1, min(g + 1, g + ln - 1), max(g, g + ln - 2)])
-    idx.update(range(max(0, wl.psi - 9), wl.psi))
-    return np.array(sorted(idx), dtype=np.int64)
-
-
-def owners_of(segs, idx):
-    """Owner rank and local index of each global index."""
-    goff = np.array([s[0] for s in segs if s[1]], dtype=np.int64)
-    own = np.array([s[2] for s in segs if s[1]], dtype=np.int64)
-    loff = np.array([s[3] for s in segs if s[1]], dtype=np.int64)
-    k = np.searchsorted(goff, idx, side="right") - 1
-    return own[k], loff[k] + (idx - goff[k])
-
-
-def gather_state(arrs, segs, idx, stage):
-    """Values of per-rank state arrays at global indices (rank 0's copy for plain data parallelism)."""
-    if stage == 0:
-        return arrs[0][torch.from_numpy(idx).to(arrs[0].device)].cpu().numpy()
-    own, loc = owners_of(segs, idx)
-    out = np.zeros(idx.size, np.float32)
-    for r in np.unique(own):
-        sel = np.nonzero(own == r)[0]
-        t = torch.from_numpy(loc[sel]).to(arrs[int(r)].device)
-        out[sel] = arrs[int(r)][t].cpu().numpy()
-    return out
-
-
-def oracle_at(wl, idx, t0=0, m=None, v=None, master=None, prior=False):
-    """The oracle's step on the sampled elements only (the step is elementwise; found is per element)."""
-    ns = idx.size
-    contiguous = ns > 0 and idx[-1] - idx[0] == ns - 1
-    if contiguous:   # a chunk of the space: the generator's contiguous path gives the same values, faster
-        grads = [synth.grads_bf16(wl, r, k, int(idx[0]), ns, prior=prior) for r in range(wl.n) for k in range(wl.a)]
-    else:
-        grads = [synth.grads_bf16_at(wl, r, k, idx, prior=prior) for r in range(wl.n) for k in range(wl.a)]
-    if master is None:
-        master = synth.master_f32(wl, int(idx[0]), ns) if contiguous else synth.master_f32_at(wl, idx)
-    M = [master.copy()]
-    Mm = [m.copy() if m is not None else np.zeros(ns, np.float32)]
-    Vv = [v.copy() if v is not None else np.zeros(ns, np.float32)]
-    M += [np.zeros(0, np.float32)] * (wl.n - 1)
-    Mm += [np.zeros(0, np.float32)] * (wl.n - 1)
-    Vv += [np.zeros(0, np.float32)] * (wl.n - 1)
-    reps = [np.zeros(ns, np.uint16) for _ in range(wl.n)]
-    res = oracle.step(ns, wl.n, wl.a, 1, [(0, ns, 0, 0)], grads, M, Mm, Vv, reps, wl.lr, wl.beta1, wl.beta2,
-                      wl.eps, wl.loss_scale, t0, threads=16)
-    return {"master": M[0], "m": Mm[0], "v": Vv[0], "replicas": reps, **res}
-
-
 def warm_state_by_oracle(b, wl, segs):
     """Warm moments from one prior step (seed + 1000) computed by the oracle for every element, chunk by
     chunk, written into the device shards; returns nothing (the device buffers hold master, m, v at t = 1)."""
     for s in range(0, wl.psi, CHUNK):
         c = min(CHUNK, wl.psi - s)
         idx = np.arange(s, s + c, dtype=np.int64)
-        o = oracle_at(wl, idx, prior=True)
+        o = gu.oracle_at(wl, idx, prior=True)
         assert o["found"] == 0
         for arr, vals in ((b.master, o["master"]), (b.m, o["m"]), (b.v, o["v"])):
             for g, ln, own, lo in segs:
@@ -123,17 +68,17 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0, mode=d
     st = dp.read_state(b.state)
     assert (st["found_inf"], st["nonfinite"], st["error"], st["t"]) == (0, 0, 0, t0 + 1)
 
-    idx = sample_indices(wl, segs, samples, wl.seed + 17)
+    idx = gu.sample_indices(wl, segs, samples, wl.seed + 17)
     if warm:
-        pr = oracle_at(wl, idx, prior=True)
-        o = oracle_at(wl, idx, t0=1, m=pr["m"], v=pr["v"], master=pr["master"])
+        pr = gu.oracle_at(wl, idx, prior=True)
+        o = gu.oracle_at(wl, idx, t0=1, m=pr["m"], v=pr["v"], master=pr["master"])
     else:
-        o = oracle_at(wl, idx)
+        o = gu.oracle_at(wl, idx)
     assert (o["found"], o["nonfinite"], o["t"]) == (0, 0, t0 + 1)
     gi = torch.from_numpy(idx).to(b.grads[0].device)
     cm, cmm, cv = b.current() if single else (b.master, b.m, b.v)
-    g = {"master": gather_state(cm, segs, idx, wl.stage), "m": gather_state(cmm, segs, idx, wl.stage),
-         "v": gather_state(cv, segs, idx, wl.stage),
+    g = {"master": gu.gather_state(cm, segs, idx, wl.stage), "m": gu.gather_state(cmm, segs, idx, wl.stage),
+         "v": gu.gather_state(cv, segs, idx, wl.stage),
          "replicas": [sd.bits_of_bf16(r[gi]) for r in b.replicas]}
     gu.assert_close_f32(g["master"], o["master"], "master")
     gu.assert_close_f32(g["m"], o["m"], "m")
@@ -154,13 +99,13 @@ def run_fullsize(wl, samples=200_000, warm=False, inject=False, repeat=0, mode=d
         # one +inf in one rank's micro-step at a seeded element: the whole step is skipped
         r, k, i, _ = synth.inject_site(wl, 0)
         b.grad(r, k)[i:i + 1].view(torch.int16).fill_(synth.BF16_POS_INF)
-        before = [gather_state(x, segs, idx, wl.stage) for x in (b.current() if single else (b.master, b.m, b.v))]
+        before = [gu.gather_state(x, segs, idx, wl.stage) for x in (b.current() if single else (b.master, b.m, b.v))]
         reps_before = [sd.bits_of_bf16(x[gi]) for x in b.replicas]
         step()
         torch.cuda.synchronize()
         st2 = dp.read_state(b.state)
         assert (st2["found_inf"], st2["nonfinite"], st2["t"]) == (1, 1, t0 + 1 + (0 if single else repeat))
-        after = [gather_state(x, segs, idx, wl.stage) for x in (b.current() if single else (b.master, b.m, b.v))]
+        after = [gu.gather_state(x, segs, idx, wl.stage) for x in (b.current() if single else (b.master, b.m, b.v))]
         for x, y in zip(before, after):
             assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
         for x, rep in zip(reps_before, b.replicas):

@@ -4,8 +4,8 @@ Some callers cannot call cudaMalloc themselves -- for example a plugin inside a 
 pre-plans all device memory, or a training loop that must not allocate once it is running.  For them
 dp_step_static keeps dp_step's scratch (the averaged-gradient shards) in a fixed array inside the library,
 so they pass only inputs and outputs.  These tests call it through the C ABI and check it against dp_step
-on two steps in a row, with the parity tolerance of the other GPU tests, and check that a layout too large
-for the array is refused before anything is launched.
+on two steps in a row, with the parity tolerance of the other GPU tests, check that a call allocates no
+device memory, and check that a layout too large for the array is refused before anything is launched.
 """
 import numpy as np
 import pytest
@@ -35,8 +35,16 @@ def test_static_scratch_step_matches_dp_step_on_two_calls(dev):
                 got.grads[q].copy_(g)
         dp.dp_step(ref.replicas, ref.master, ref.m, ref.v, ref.grads, wl.a, c.layout, A, wl.loss_scale,
                    gbar_shard=ref.gbar, state=ref.state)
+        torch.cuda.synchronize()
+        free0, reserved0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved()
         dp.dp_step_static(got.replicas, got.master, got.m, got.v, got.grads, wl.a, c.layout, A, wl.loss_scale,
                           state=got.state)
+        torch.cuda.synchronize()
+        # No call allocates: the device's free memory and torch's pool are unchanged by the call.  (The first
+        # call on a device may load the library's module that holds the array; later calls change nothing.)
+        assert torch.cuda.memory_reserved() == reserved0
+        if call == 1:
+            assert torch.cuda.mem_get_info()[0] == free0
         r, g = gu.gpu_result(c, ref), gu.gpu_result(c, got)
         assert (g["found"], g["nonfinite"], g["t"], g["error"]) == (r["found"], r["nonfinite"], r["t"], r["error"])
         assert g["t"] == call + 1

@@ -45,7 +45,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs
+    cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs + ["-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc link failed:\n%s\n%s" % (r.stdout, r.stderr))

@@ -353,6 +353,7 @@ dp_status_t dp_accumulate(float* const* acc, const uint16_t* const* g, int64_t p
   if (st != DP_OK) return st;
   if (psi == 0) return DP_OK;
   LaunchCount lc;
+  dp::NvtxRange range("dpstep accumulate");
   cudaError_t e = dp::launch_accumulate(acc, g, psi, n, first, arith, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "accumulate launch");
 }
@@ -368,6 +369,7 @@ dp_status_t dp_reduce_scatter_avg(float* const* gbar_shard, const float* const* 
   if ((st = check_full_arrays(P, (const void* const*)acc, P.n, "acc")) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
+  dp::NvtxRange range("dpstep reduce-scatter + average + check");
   cudaError_t e = s.order == DP_ORDER_TREE
                       ? dp::launch_rs_tree(P, acc, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n)
                       : dp::launch_rs_avg(P, acc, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n);
@@ -386,6 +388,7 @@ dp_status_t dp_adam_shard(float* const* master, float* const* m, float* const* v
   if ((st = check_ptr_array((const void* const*)gbar_shard, P.n, "gbar_shard", P.shard_len)) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
+  dp::NvtxRange range("dpstep adam shard");
   cudaError_t e = dp::launch_advance(d_state, (double)adam.beta1, (double)adam.beta2, (cudaStream_t)stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "advance launch");
   e = dp::launch_update(P, nullptr, master, m, v, gbar_shard, s, d_state, (cudaStream_t)stream, &lc.n);
@@ -405,6 +408,7 @@ dp_status_t dp_allgather_params(uint16_t* const* replicas, const float* const* m
   }
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
+  dp::NvtxRange range("dpstep all-gather params");
   cudaError_t e = dp::launch_allgather(P, replicas, master, d_state, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "allgather launch");
 }
@@ -425,8 +429,16 @@ static dp_status_t prepare_reduce(const Plan& P, const uint16_t* const* grads, i
 // the same operations, p = g_{s+1} + ... + g_s then gbar; the ring kernel streams faster.)
 static cudaError_t launch_pass_a(const Plan& P, const uint16_t* const* grads, int a, float* const* gb,
                                  const StepScalars& s, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  dp::NvtxRange range("dpstep pass A: accumulate, reduce-scatter, average, check");
   if (s.order == DP_ORDER_TREE) return dp::launch_reduce_tree(P, grads, a, gb, s, 1, st, stream, launches);
   return dp::launch_reduce(P, grads, a, gb, s, 1, st, stream, launches);
+}
+
+static cudaError_t launch_pass_b(const Plan& P, uint16_t* const* rep, float* const* master, float* const* m,
+                                 float* const* v, const float* const* gb, const StepScalars& s,
+                                 const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
+  dp::NvtxRange range("dpstep pass B: adam, all-gather");
+  return dp::launch_update(P, rep, master, m, v, gb, s, st, stream, launches);
 }
 
 dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* const* grads, int32_t a,
@@ -465,6 +477,7 @@ dp_status_t dp_reduce_scatter_micro(float* const* acc_shard, float* const* gbar_
   if (k == a - 1 && (st = gbar_ptrs(P, gbar_shard, ws, gb)) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
+  dp::NvtxRange range("dpstep micro-step reduce-scatter");
   cudaError_t e = dp::launch_rs_micro(P, g, a > 1 ? acc_shard : nullptr, gb, k, a, s, d_state, (cudaStream_t)stream,
                                       &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "reduce_scatter_micro launch");
@@ -484,7 +497,7 @@ dp_status_t dp_step_update(uint16_t* const* replicas, float* const* master, floa
   if ((st = gbar_ptrs(P, (float* const*)gbar_shard, ws, gb)) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
-  cudaError_t e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
+  cudaError_t e = launch_pass_b(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
 }
 
@@ -513,6 +526,7 @@ dp_status_t step_impl(uint16_t* const* replicas, float* const* master, float* co
     return st;
   const size_t bytes = (size_t)P.psi * sizeof(uint16_t);
   if (host_grads && bytes) {
+    dp::NvtxRange range("dpstep gradient copies to the device");
     for (int q = 0; q < P.n * a; ++q) {
       const cudaError_t e = cudaMemcpyAsync(const_cast<uint16_t*>(grads[q]), host_grads[q], bytes,
                                             cudaMemcpyHostToDevice, stream);
@@ -522,7 +536,7 @@ dp_status_t step_impl(uint16_t* const* replicas, float* const* master, float* co
   LaunchCount lc;
   cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
-  e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, stream, &lc.n);
+  e = launch_pass_b(P, replicas, master, m, v, gb, s, d_state, stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "update launch");
   if (host_state) {
     e = cudaMemcpyAsync(host_state, d_state, sizeof(dp_step_state_t), cudaMemcpyDeviceToHost, stream);
@@ -587,7 +601,7 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
   LaunchCount lc;
   cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
-  e = dp::launch_update(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
+  e = launch_pass_b(P, replicas, master, m, v, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
 }
 
@@ -612,6 +626,7 @@ dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master,
   if ((st = check_ptr_array((const void* const*)v, 2 * P.n, "v (2 sets)", lens2)) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
   LaunchCount lc;
+  dp::NvtxRange range("dpstep single pass: reduce, adam, all-gather");
   cudaError_t e = dp::launch_single_pass(P, grads, a, replicas, master, m, v, s, d_state, (cudaStream_t)stream,
                                          &lc.n);
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "single-pass launch");

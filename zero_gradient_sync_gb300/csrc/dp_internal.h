@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "dp_device.cuh"
@@ -29,6 +30,15 @@ struct StepScalars {
   int32_t order;  // DP_ORDER_RING or DP_ORDER_TREE
   uint64_t timeout_ns;
   ScalerK scaler;  // disabled unless the step uses the device-resident loss scale
+};
+
+// A named range on the host timeline around the launches of one phase of the step (pass A, pass B, ...), so a
+// trace splits a step into its phases; costs nothing unless a profiler is attached (NVTX v3, header-only).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 // Records msg as this thread's dp_last_error() and returns s.

@@ -16,7 +16,6 @@
 // Nothing in it has to start at zero -- the reduce kernel writes every
 // scratch element it later reads -- so it is never cleared.
 #include <cstdio>
-#include <mutex>
 
 #include "dp_device.cuh"
 #include "dp_internal.h"
@@ -28,24 +27,15 @@ static __device__ __align__(256) unsigned char g_static_scratch[DP_STATIC_SCRATC
 
 namespace {
 
-// Device address of g_static_scratch, looked up once per device with that device current.
-// In host code the symbol itself only names a host-side shadow, never the device memory.
-std::mutex g_addr_mu;
-void* g_addr[64] = {nullptr};
-
+// Device address of g_static_scratch in the context current on this thread.  In host code the symbol itself
+// only names a host-side shadow, never the device memory, so every call asks the runtime for the address:
+// the lookup is cheap, and a cached address would go stale when the context changes under the same device
+// number (a cudaDeviceReset, or another context made current on the device).
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_addr[dev] = p;
-  }
-  *out = g_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 
