@@ -4,16 +4,22 @@
 
 One step = the whole hot path over one batch of synthetic inputs: n*a bf16 micro-step gradients accumulated,
 reduced in ring order, averaged, unscaled and finite-checked, partitioned Adam on the fp32 shards, and the bf16
-all-gather into the n replicas (dp_step_reduce + dp_step_update, the two kernels of dp_step).  The default
-workload is the GPT-2-small parameter list (123,568,896 params), n=8, a=4, ZeRO-1 even shards, loss scale 2^16.
+all-gather into the n replicas.  By default the step is dp_step_single_pass (one reduce-and-update pass over
+double-buffered optimizer state, the fastest path); --path two-pass times dp_step's two kernels
+(dp_step_reduce + dp_step_update), --path microstep the per-micro-step reduce-scatter + dp_step_update.  The
+default workload is the GPT-2-small parameter list (123,568,896 params), n=8, a=4, ZeRO-1 even shards, loss scale
+2^16.  hbm_gbs counts the single-pass algorithmic minimum B1 = 2na + 24 + 2n bytes per parameter for every
+path; hbm_gbs_path_bytes counts the bytes the timed path's own design moves (B1 + 8 for the two-pass step).
 
-The end-to-end leg ("e2e") times dp_step_from_host: every step's gradients copied from pinned host memory, the
-step, and the 64-byte step state read back, in one C-ABI call.  --path single-pass / microstep time
-dp_step_single_pass or the per-micro-step reduce-scatter instead; --order tree the binomial-tree order;
---workload also takes the flat sweep's case names (sweep_<psi>_n<n>_a<a>_<even|ragged>).
+The end-to-end leg ("e2e") times the same step through one C-ABI call with the gradients in host memory
+(dp_step_single_pass_from_host, or dp_step_from_host for --path two-pass): every step's gradients copied from
+pinned host memory, the step, and the 64-byte step state read back.  --order tree times the binomial-tree order
+(two-pass path); --workload also takes the flat sweep's case names (sweep_<psi>_n<n>_a<a>_<even|ragged>).
 
-Multi-GPU (torchrun): the path does not shard across GPUs; every rank runs an independent replica of the
-workload (weak scaling), with a barrier and max-over-ranks timing and no collective in the data path.
+Multi-GPU (torchrun): every rank holds one workload-sized slice of an N-times-larger parameter space (weak
+scaling) and runs the sliced step: its reduction with the commit deferred, one 4-byte NCCL all-reduce (MAX) of
+the skip flag, then the commit and the update -- the one collective of a step split across GPUs.  Barrier and
+max-over-ranks timing.
 
 Rank 0 prints one JSON line.  --impl reference times the float64 CPU oracle on the host cores instead.
 """
@@ -54,10 +60,14 @@ def parse():
                         "directory instead of the step (prints its own JSON line)")
     p.add_argument("--order", choices=["ring", "tree"], default="ring",
                    help="order of the ranks' sums: the ring reduce-scatter's, or a binomial tree's")
-    p.add_argument("--path", choices=["two-pass", "single-pass", "microstep"], default="two-pass",
-                   help="dp_step (reduce + update kernels), dp_step_single_pass (one pass, two state sets) or "
-                        "dp_reduce_scatter_micro per micro-step + dp_step_update (the ZeRO-2 form)")
-    return p.parse_args()
+    p.add_argument("--path", choices=["two-pass", "single-pass", "microstep"], default=None,
+                   help="dp_step_single_pass (one pass, two state sets; the default), dp_step (reduce + update "
+                        "kernels; the default with --order tree) or dp_reduce_scatter_micro per micro-step + "
+                        "dp_step_update (the ZeRO-2 form)")
+    args = p.parse_args()
+    if args.path is None:
+        args.path = "two-pass" if args.order == "tree" else "single-pass"
+    return args
 
 
 def dist_env():
@@ -298,6 +308,7 @@ def native_main(args, wl):
     import synth
     import zero_gradient_sync_gb300 as dp
     from synth import device as sd
+    from zero_gradient_sync_gb300 import sliced
     from zero_gradient_sync_gb300.buffers import StepBuffers
 
     ws, rank, local = dist_env()
@@ -307,6 +318,13 @@ def native_main(args, wl):
         tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
     else:
         torch.cuda.set_device(0)
+    # N > 1: this rank's workload is its slice of an N-times-larger space; the slices share one skip decision.
+    split = ws > 1
+
+    def combine_max(flag):
+        import torch.distributed as tdist
+        tdist.all_reduce(flag, op=tdist.ReduceOp.MAX)
+
     dev = torch.device("cuda", torch.cuda.current_device())
     mode = dp.DP_SUM_COMPENSATED if args.sum == "compensated" else dp.DP_SUM_PLAIN
     tree = args.order == "tree"
@@ -320,6 +338,10 @@ def native_main(args, wl):
     micro = args.path == "microstep"
     if micro and tree:
         raise SystemExit("--path microstep runs in ring order only")
+    if micro and split:
+        raise SystemExit("--path microstep runs on one GPU")
+    if single and wl.stage == 0:
+        raise SystemExit("the single pass takes ZeRO stages 1-3; use --path two-pass for stage 0")
     bufs = StepBuffers(layout, wl.a, dev, second_set=single, micro_acc=micro)
     A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
 
@@ -341,14 +363,30 @@ def native_main(args, wl):
 
     stream = torch.cuda.current_stream()
 
-    def one_step():
-        if single:
+    flag_ops = sliced.LibraryOps()
+
+    def first_half():
+        """The timed kernel of the roofline: the single pass, the a per-micro-step launches, or pass A."""
+        if split:
+            sliced.reduce_deferred(bufs, A, wl.loss_scale, mode, single_pass=single)
+        elif single:
             bufs.step_single_pass(A, wl.loss_scale, mode)
         elif micro:
-            bufs.step_micro(A, wl.loss_scale, mode)
+            for kk in range(wl.a):
+                bufs.reduce_micro(kk, A, wl.loss_scale, mode)
         else:
             bufs.reduce(A, wl.loss_scale, mode)
+
+    def second_half():
+        if split:
+            combine_max(flag_ops.found_flag(bufs))
+            sliced.commit_and_update(bufs, A, single_pass=single)
+        elif not single:
             bufs.update(A)
+
+    def one_step():
+        first_half()
+        second_half()
 
     for _ in range(args.warmup):
         one_step()
@@ -368,18 +406,9 @@ def native_main(args, wl):
     clocks.mark(0)
     for k in range(K):
         ev[k][0].record(stream)
-        if single:
-            bufs.step_single_pass(A, wl.loss_scale, mode)
-            ev[k][1].record(stream)
-        elif micro:
-            for kk in range(wl.a):
-                bufs.reduce_micro(kk, A, wl.loss_scale, mode)
-            ev[k][1].record(stream)
-            bufs.update(A)
-        else:
-            bufs.reduce(A, wl.loss_scale, mode)
-            ev[k][1].record(stream)
-            bufs.update(A)
+        first_half()
+        ev[k][1].record(stream)
+        second_half()
     end.record(stream)
     torch.cuda.synchronize()
     clocks.mark(1)
@@ -405,13 +434,15 @@ def native_main(args, wl):
     upd_avg = sum(upd_ms) / K
     red_ach = red_bytes * wl.psi / (red_avg * 1e-3) / 1e9
     upd_ach = upd_bytes * wl.psi / max(1e-9, upd_avg * 1e-3) / 1e9
-    step_gbs = (b1 if single else (red_bytes + upd_bytes) if micro else b2) * wl.psi / (ms * 1e-3) / 1e9
+    path_bytes = b1 if single else (red_bytes + upd_bytes) if micro else b2
+    step_gbs = b1 * wl.psi / (ms * 1e-3) / 1e9           # the single-pass algorithmic minimum, every path
+    path_gbs = path_bytes * wl.psi / (ms * 1e-3) / 1e9    # what the timed path's own design moves
     traffic = recorded_traffic(wl.name, "single_pass" if single else "rs_micro" if micro else
                                ("reduce_tree" if tree else "reduce"))
 
     # End to end through the public call with host buffers: the step's gradients copied from pinned host
-    # memory, the step, and the step's status read back, every step -- for the two-pass step one C-ABI call,
-    # dp_step_from_host, does all three.
+    # memory, the step, and the step's status read back, every step -- one C-ABI call does all three
+    # (dp_step_single_pass_from_host, or dp_step_from_host for the two-pass step).
     e2e = None
     if not args.no_e2e:
         KE = args.e2e_steps or min(K, 20)
@@ -420,16 +451,20 @@ def native_main(args, wl):
         s1 = torch.cuda.Event(enable_timing=True)
 
         def e2e_step():
-            if not single and not micro:
-                bufs.step_from_host(host_grads, A, wl.loss_scale, mode, host_state=host_state)
-                return
-            for q, h in enumerate(host_grads):
-                bufs.grads[q].view(torch.int16).copy_(h, non_blocking=True)
-            if single:
-                bufs.step_single_pass(A, wl.loss_scale, mode)
-            else:
+            if split:
+                for q, h in enumerate(host_grads):
+                    bufs.grads[q].view(torch.int16).copy_(h, non_blocking=True)
+                one_step()
+                host_state.copy_(bufs.state, non_blocking=True)
+            elif single:
+                bufs.step_single_pass_from_host(host_grads, A, wl.loss_scale, mode, host_state=host_state)
+            elif micro:
+                for q, h in enumerate(host_grads):
+                    bufs.grads[q].view(torch.int16).copy_(h, non_blocking=True)
                 bufs.step_micro(A, wl.loss_scale, mode)
-            host_state.copy_(bufs.state, non_blocking=True)
+                host_state.copy_(bufs.state, non_blocking=True)
+            else:
+                bufs.step_from_host(host_grads, A, wl.loss_scale, mode, host_state=host_state)
 
         # Untimed warm-up of this leg too: the first host-to-device copy from freshly pinned pages has measured
         # ~250 ms on its own for the 7.9 GB of the GPT-2 workload (a one-time mapping cost), against 37.5 ms after.
@@ -471,8 +506,11 @@ def native_main(args, wl):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded Philox4x64 N(0, sigma) bf16 gradients, fp32 master; no dataset)",
             "config": config_of(wl, args),
-            "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak, "hbm_peak_gbs": peak,
-            "hbm_peak_kind": peak_kind,
+            "hbm_gbs": step_gbs, "hbm_frac_of_peak": step_gbs / peak, "hbm_frac_of_nominal_7900": step_gbs / 7900.0,
+            "hbm_bytes_per_param": b1, "hbm_gbs_path_bytes": path_gbs, "path_bytes_per_param": path_bytes,
+            "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+            "split": ({"slices": ws, "collective": "4-byte NCCL all-reduce (MAX) of found_inf per step"}
+                      if split else None),
             "roofline": {"bound": "hbm",
                          "kernel": ("single-pass reduce + Adam + all-gather" if single else
                                     "per-micro-step reduce-scatter (a launches per step, summed)" if micro else
@@ -481,8 +519,10 @@ def native_main(args, wl):
                          "achieved": red_ach, "peak": peak, "unit": "GB/s", "frac": red_ach / peak,
                          "traffic": traffic, "bytes_per_launch": red_bytes * wl.psi, "avg_ms": red_avg,
                          "peak_kind": peak_kind},
-            "kernels": ({"single_pass": {"avg_ms": red_avg, "gbs": red_ach, "bytes_per_param": red_bytes},
-                         "repair": {"avg_ms": upd_avg}} if single else
+            "kernels": ({"single_pass": {"avg_ms": red_avg, "gbs": red_ach, "bytes_per_param": red_bytes,
+                                         "note": "events bracket the fused kernel and the repair launch, which "
+                                                 "returns at once on an applied step"},
+                         "after": {"avg_ms": upd_avg}} if single else
                         {("rs_micro" if micro else "reduce"): {"avg_ms": red_avg, "gbs": red_ach,
                                                                 "bytes_per_param": red_bytes},
                          "update": {"avg_ms": upd_avg, "gbs": upd_ach, "bytes_per_param": upd_bytes}}),

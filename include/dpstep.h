@@ -96,6 +96,25 @@ enum {
  *     steps.)  dp_step_single_pass takes the ring order only. */
 enum { DP_ORDER_RING = 0, DP_ORDER_TREE = 16 };
 
+/* Step flags, OR'd into sum_mode, for a step split across several GPUs, each
+ * holding one contiguous slice of the parameter space with all n ranks' data
+ * for it (dp_layout_slice).  Every step of the path is elementwise except the
+ * skip decision, which must be global: a non-finite value in any slice skips
+ * the step on every slice ("Distributed Training: Split along the Four Axes",
+ * data-parallel paragraph: every rank applies the same update, so replicas
+ * stay identical).  Accepted by dp_step_reduce, dp_step_single_pass(_from_host)
+ * and dp_reduce_scatter_micro; the other calls refuse them.
+ *   DP_DEFER_COMMIT: the reduction publishes found_inf / nonfinite for its own
+ *     slice but leaves t, the beta powers, the current state set and the loss
+ *     scale alone.  The caller combines found_inf (the int32 at byte offset 4
+ *     of dp_step_state_t) over the slices with a maximum -- one 4-byte
+ *     all-reduce -- and then calls dp_commit_step (before dp_step_update) or
+ *     dp_commit_single_pass.
+ *   DP_DEVICE_SCALE: the reduction unscales by d_state->loss_scale (checked on
+ *     the device as dp_step_scaled checks it) instead of the loss_scale
+ *     argument, which is then not used; the commit applies the scale policy. */
+enum { DP_DEFER_COMMIT = 32, DP_DEVICE_SCALE = 64 };
+
 /* ZeRO stages of the layout. */
 enum { DP_STAGE_DP = 0, DP_STAGE_ZERO1 = 1, DP_STAGE_ZERO2 = 2, DP_STAGE_ZERO3 = 3 };
 
@@ -192,6 +211,22 @@ dp_status_t dp_layout_validate(const dp_layout_t* layout);
  * *nseg is the capacity on entry and the number of segments on return. */
 dp_status_t dp_layout_even(int64_t psi, int32_t n, int64_t bucket, int32_t misalign, dp_segment_t* out,
                            int32_t* nseg);
+
+/* The part of a layout inside the global range [lo, hi) of its parameter
+ * space, as a layout of its own: the slice one GPU holds when the space is
+ * split into contiguous slices (the step flags above).  Segment pieces inside
+ * [lo, hi) in order, with global_off rebased to lo and local_off rebased to
+ * local_base[owner], the lowest local index of that owner's pieces in the
+ * slice (0 for an owner with none); the slice layout has psi = hi - lo, the
+ * same stage and n.  So the slice's shard array of rank s holds elements
+ * [local_base[s], local_base[s] + dp_shard_len(slice, s)) of rank s's whole
+ * shard array (stage 0: elements [lo, hi) of the full arrays), and its
+ * gradient and replica buffers hold elements [lo, hi).  out may be NULL to
+ * query the count: *nseg is the capacity on entry and the count on return;
+ * local_base (n entries) may be NULL.  Not on the pages: a host-side layout
+ * helper.  DP_ERR_INVALID_ARG for a bad layout or range. */
+dp_status_t dp_layout_slice(const dp_layout_t* layout, int64_t lo, int64_t hi, dp_segment_t* out, int32_t* nseg,
+                            int64_t* local_base);
 
 /* Local length of rank's shard arrays (end of its furthest segment); -1 on
  * error.  Not on the pages: a size query of the layout above. */
@@ -293,7 +328,8 @@ dp_status_t dp_reduce_scatter_avg(float* const* gbar_shard, const float* const* 
  *   local index; the caller's memory, overwritten at k = 0; unused (may be
  *   NULL) when a = 1.
  * gbar_shard / ws: as for dp_step_reduce; used by the k = a-1 call only.
- * Ring order only (DP_ORDER_TREE is DP_ERR_INVALID_ARG). */
+ * Ring order only (DP_ORDER_TREE is DP_ERR_INVALID_ARG).  Accepts
+ * DP_DEFER_COMMIT and DP_DEVICE_SCALE (they act on the k = a-1 call). */
 dp_status_t dp_reduce_scatter_micro(float* const* acc_shard, float* const* gbar_shard, void* ws,
                                     const uint16_t* const* g, int32_t k, int32_t a, const dp_layout_t* layout,
                                     dp_adam_t adam, float loss_scale, int32_t sum_mode, dp_step_state_t* d_state,
@@ -369,7 +405,8 @@ dp_status_t dp_step_from_host(uint16_t* const* replicas, float* const* master, f
  * accumulate + ring reduce-scatter +
  * average + unscale + non-finite check, gbar into the shards; the last CTA
  * publishes found_inf / nonfinite and, unless found, advances t and the
- * beta powers for the update that follows. */
+ * beta powers for the update that follows.  Accepts DP_DEFER_COMMIT and
+ * DP_DEVICE_SCALE in sum_mode. */
 dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* const* grads, int32_t a,
                            const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
                            dp_step_state_t* d_state, dp_stream_t stream);
@@ -417,10 +454,45 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
  * kernel rewrites them as bf16_rne of the (unchanged) current master, so a
  * skipped step leaves the replicas as they were provided they held
  * bf16_rne(master) before it -- the invariant every applied step
- * establishes.  Results are bit-identical to dp_step.  Stages 1-3 only. */
+ * establishes.  Results are bit-identical to dp_step.  Stages 1-3 only.
+ * Accepts DP_DEFER_COMMIT (then only the pass is launched; the state set is
+ * not flipped and the replicas not repaired until dp_commit_single_pass) and
+ * DP_DEVICE_SCALE in sum_mode. */
 dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
                                 const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
                                 float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream);
+
+/* dp_step_single_pass with the step's gradients in host memory, like
+ * dp_step_from_host: on `stream`, the n*a host buffers host_grads[q] are
+ * copied into the device buffers grads[q] (one cudaMemcpyAsync each), the
+ * single pass runs on them, and, if host_state is not NULL, the 64-byte state
+ * is copied back to host_state.  Arguments are checked before anything is
+ * queued; host buffers should be pinned and stay valid until the stream has
+ * passed the copies.  Results are those of dp_step_single_pass.  (Same
+ * passages as dp_step; the copies are not on the pages.) */
+dp_status_t dp_step_single_pass_from_host(uint16_t* const* replicas, float* const* master, float* const* m,
+                                          float* const* v, const uint16_t* const* host_grads, uint16_t* const* grads,
+                                          int32_t a, const dp_layout_t* layout, dp_adam_t adam, float loss_scale,
+                                          int32_t sum_mode, dp_step_state_t* d_state, dp_step_state_t* host_state,
+                                          dp_stream_t stream);
+
+/* Commits a step whose reduction ran with DP_DEFER_COMMIT, once found_inf in
+ * *d_state holds the decision of every slice (the caller's maximum over the
+ * slices): unless found_inf (or a recorded device error), t += 1 and the beta
+ * powers advance with adam.beta1 / beta2; with a scaler, the device-resident
+ * loss scale then follows its policy (see dp_scaler_t), NULL leaves it.  One
+ * kernel; call dp_step_update after it.  ("Distributed Training: Split along
+ * the Four Axes", data-parallel paragraph: all ranks apply one update.) */
+dp_status_t dp_commit_step(dp_step_state_t* d_state, dp_adam_t adam, const dp_scaler_t* scaler, dp_stream_t stream);
+
+/* dp_commit_step for dp_step_single_pass with DP_DEFER_COMMIT: the commit also
+ * makes the set the pass wrote current unless found_inf, and on a skipped step
+ * rewrites the replicas from the (unchanged) current master, as the single
+ * pass's own repair does.  replicas, master (2n pointers) and layout as for
+ * dp_step_single_pass.  Two kernels. */
+dp_status_t dp_commit_single_pass(uint16_t* const* replicas, float* const* master, const dp_layout_t* layout,
+                                  dp_adam_t adam, const dp_scaler_t* scaler, dp_step_state_t* d_state,
+                                  dp_stream_t stream);
 
 /* Reads found_inf and error of *d_state into host ints after synchronising
  * the stream (the one blocking call).  skipped / err may be NULL.  Not on the

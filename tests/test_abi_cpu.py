@@ -204,3 +204,69 @@ def test_status_strings_and_timeout_knob(dp):
     dp.dp_set_wait_timeout_ns(12345)
     assert dp.dp_get_wait_timeout_ns() == 12345
     dp.dp_set_wait_timeout_ns(old)
+
+
+@pytest.mark.parametrize("kind", ["even", "buckets", "ragged", "random"])
+def test_layout_slice_maps_every_element(dp, kind):
+    """dp_layout_slice: every element of [lo, hi) keeps its owner, and its local index in the slice plus the
+    owner's local_base is its local index in the whole layout (checked element by element)."""
+    import synth
+    psi, n = 9_973, 5
+    wl = synth.WORKLOADS["tiny"].with_(psi=psi, n=n, layout=kind, bucket=1_001, misalign=3, nseg=37, seed=5)
+    segs = synth.layout_of(wl)
+    L = dp.Layout(3, n, psi, segs)
+    own = np.empty(psi, np.int64)
+    loc = np.empty(psi, np.int64)
+    for g, ln, o, lo in segs:
+        own[g:g + ln] = o
+        loc[g:g + ln] = lo + np.arange(ln)
+    rng = np.random.default_rng(3)
+    cuts = [(0, psi), (0, 0), (psi, psi), (1, 2), (17, 5_000), (4_999, psi)]
+    cuts += [tuple(sorted(rng.integers(0, psi + 1, 2).tolist())) for _ in range(6)]
+    for lo, hi in cuts:
+        S, base = L.slice(lo, hi)
+        S.validate()
+        assert S.psi == hi - lo and S.n == n and S.stage == 3
+        got_own = np.full(hi - lo, -1, np.int64)
+        got_loc = np.full(hi - lo, -1, np.int64)
+        for g, ln, o, l0 in S.segs:
+            got_own[g:g + ln] = o
+            got_loc[g:g + ln] = base[o] + l0 + np.arange(ln)
+        assert np.array_equal(got_own, own[lo:hi])
+        assert np.array_equal(got_loc, loc[lo:hi])
+        for r in range(n):   # each slice shard starts at the owner's lowest local index in the slice
+            mine = loc[lo:hi][own[lo:hi] == r]
+            assert base[r] == (mine.min() if mine.size else 0)
+    with pytest.raises(dp.DPError):
+        L.slice(5, 3)
+    with pytest.raises(dp.DPError):
+        L.slice(0, psi + 1)
+
+
+def test_step_flags_accepted_only_where_documented(dp):
+    """DP_DEFER_COMMIT / DP_DEVICE_SCALE: the calls that cannot defer refuse them before any launch; the
+    commit calls check their arguments on the host."""
+    L = dp.Layout(1, 2, 16, [(0, 8, 0, 0), (8, 8, 1, 0)])
+    A = dp.adam()
+    fake = [16 * (k + 1) for k in range(8)]
+    before = dp.dp_kernel_launches()
+    for flag in (dp.DP_DEFER_COMMIT, dp.DP_DEVICE_SCALE):
+        with pytest.raises(dp.DPError) as e:
+            dp.dp_step(fake[:2], fake[:2], fake[:2], fake[:2], fake[:2], 1, L, A, 1.0, sum_mode=flag,
+                       gbar_shard=fake[:2], state=256, stream=0)
+        assert e.value.code == dp.DP_ERR_INVALID_ARG and "not accepted" in str(e.value)
+        with pytest.raises(dp.DPError):
+            dp.dp_step_scaled(fake[:2], fake[:2], fake[:2], fake[:2], fake[:2], 1, L, A, dp.scaler(), sum_mode=flag,
+                              gbar_shard=fake[:2], state=256, stream=0)
+        with pytest.raises(dp.DPError):
+            dp.dp_reduce_scatter_avg(fake[:2], fake[:2], L, 1.0, flag, 256, stream=0)
+    with pytest.raises(dp.DPError):              # an unknown bit
+        dp.dp_step_reduce(fake[:2], None, fake[:2], 1, L, A, 1.0, 128, 256, stream=0)
+    with pytest.raises(dp.DPError):              # commit: null state
+        dp.dp_commit_step(0, A, stream=0)
+    with pytest.raises(dp.DPError):              # commit: bad scaler
+        dp.dp_commit_step(256, A, dp.scaler(growth_factor=0.5), stream=0)
+    with pytest.raises(dp.DPError):              # single-pass commit: stage 0
+        dp.dp_commit_single_pass(fake[:2], fake[:4], dp.Layout(0, 2, 16, [(0, 8, 0, 0), (8, 8, 1, 0)]), A, 256,
+                                 stream=0)
+    assert dp.dp_kernel_launches() == before

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(HERE, "libdpstep.so")
 DP_OK, DP_ERR_INVALID_ARG, DP_ERR_ALIGNMENT, DP_ERR_CUDA, DP_ERR_TIMEOUT, DP_ERR_IO = 0, 1, 2, 3, 4, 5
 DP_SUM_COMPENSATED, DP_SUM_PLAIN = 0, 1
 DP_ORDER_RING, DP_ORDER_TREE = 0, 16   # OR'd into sum_mode
+DP_DEFER_COMMIT, DP_DEVICE_SCALE = 32, 64   # step flags, OR'd into sum_mode
 DP_MAX_N, DP_MAX_NA, DP_MAX_SEG = 16, 64, 1024
 STATE_BYTES = 64
 
@@ -64,6 +65,11 @@ def _load() -> ctypes.CDLL:
         "dp_last_error": (ctypes.c_char_p, []),
         "dp_layout_validate": (c_i32, [P(dp_layout_t)]),
         "dp_layout_even": (c_i32, [c_i64, c_i32, c_i64, c_i32, P(dp_segment_t), P(c_i32)]),
+        "dp_layout_slice": (c_i32, [P(dp_layout_t), c_i64, c_i64, P(dp_segment_t), P(c_i32), P(c_i64)]),
+        "dp_commit_step": (c_i32, [c_vp, dp_adam_t, P(dp_scaler_t), c_vp]),
+        "dp_commit_single_pass": (c_i32, [c_vp, c_vp, P(dp_layout_t), dp_adam_t, P(dp_scaler_t), c_vp, c_vp]),
+        "dp_step_single_pass_from_host": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, P(dp_layout_t), dp_adam_t,
+                                                  c_f32, c_i32, c_vp, c_vp, c_vp]),
         "dp_shard_len": (c_i64, [P(dp_layout_t), c_i32]),
         "dp_workspace_size": (ctypes.c_size_t, [P(dp_layout_t)]),
         "dp_acc_elems": (ctypes.c_size_t, [c_i64, c_i32]),
@@ -205,6 +211,17 @@ class Layout:
     def workspace_size(self) -> int:
         return int(LIB.dp_workspace_size(ctypes.byref(self.c)))
 
+    def slice(self, lo: int, hi: int) -> Tuple["Layout", List[int]]:
+        """The part of this layout inside global [lo, hi) as a layout of its own (dp_layout_slice), and each
+        rank's local_base: where the slice's shard array starts in that rank's whole shard array."""
+        cnt = c_i32(0)
+        _check(LIB.dp_layout_slice(ctypes.byref(self.c), lo, hi, None, ctypes.byref(cnt), None), "dp_layout_slice")
+        arr = (dp_segment_t * max(1, cnt.value))()
+        base = (c_i64 * max(1, self.n))()
+        _check(LIB.dp_layout_slice(ctypes.byref(self.c), lo, hi, arr, ctypes.byref(cnt), base), "dp_layout_slice")
+        segs = [(arr[k].global_off, arr[k].len, arr[k].owner, arr[k].local_off) for k in range(cnt.value)]
+        return Layout(self.stage, self.n, hi - lo, segs), [int(base[r]) for r in range(self.n)]
+
 
 def adam(lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8) -> dp_adam_t:
     return dp_adam_t(lr, beta1, beta2, eps)
@@ -268,6 +285,21 @@ def dp_step(replicas, master, m, v, grads, a: int, layout: Layout, adam_: dp_ada
            "dp_step")
 
 
+def _host_args(layout: Layout, host_grads, grads, host_state):
+    """Host gradient pointer array and host state address of the *_from_host calls."""
+    if len(host_grads) != len(grads):
+        raise ValueError("host_grads: %d buffers for %d device buffers" % (len(host_grads), len(grads)))
+    for i, h in enumerate(host_grads):
+        if h.is_cuda or h.element_size() != 2 or not h.is_contiguous() or h.numel() < layout.psi:
+            raise ValueError("host_grads[%d] must be a contiguous CPU tensor of >= psi 2-byte elements" % i)
+    hs = 0
+    if host_state is not None:
+        if host_state.is_cuda or host_state.numel() * host_state.element_size() < STATE_BYTES:
+            raise ValueError("host_state must be a CPU tensor of at least %d bytes" % STATE_BYTES)
+        hs = host_state.data_ptr()
+    return (c_vp * max(1, len(host_grads)))(*[h.data_ptr() for h in host_grads]), hs
+
+
 def dp_step_from_host(replicas, master, m, v, host_grads, grads, a: int, layout: Layout, adam_: dp_adam_t,
                       loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED, gbar_shard=None, ws=None, state=None,
                       host_state=None, stream=None) -> None:
@@ -279,17 +311,7 @@ def dp_step_from_host(replicas, master, m, v, host_grads, grads, a: int, layout:
         _check_tensors(ts, 4, lens, name)
     _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
     _check_tensors(grads, 2, [layout.psi] * len(grads), "grads")
-    if len(host_grads) != len(grads):
-        raise ValueError("host_grads: %d buffers for %d device buffers" % (len(host_grads), len(grads)))
-    for i, h in enumerate(host_grads):
-        if h.is_cuda or h.element_size() != 2 or not h.is_contiguous() or h.numel() < layout.psi:
-            raise ValueError("host_grads[%d] must be a contiguous CPU tensor of >= psi 2-byte elements" % i)
-    hs = 0
-    if host_state is not None:
-        if host_state.is_cuda or host_state.numel() * host_state.element_size() < STATE_BYTES:
-            raise ValueError("host_state must be a CPU tensor of at least %d bytes" % STATE_BYTES)
-        hs = host_state.data_ptr()
-    hp = (c_vp * max(1, len(host_grads)))(*[h.data_ptr() for h in host_grads])
+    hp, hs = _host_args(layout, host_grads, grads, host_state)
     gb, w = _gbar_args(layout, gbar_shard, ws)
     _check(LIB.dp_step_from_host(_ptr_array(replicas), _ptr_array(master), _ptr_array(m), _ptr_array(v), hp,
                                  _ptr_array(grads), a, ctypes.byref(layout.c), adam_, loss_scale, sum_mode, gb, w,
@@ -343,6 +365,44 @@ def dp_step_single_pass(replicas, master2, m2, v2, grads, a: int, layout: Layout
     _check(LIB.dp_step_single_pass(_ptr_array(replicas), _ptr_array(master2), _ptr_array(m2), _ptr_array(v2),
                                    _ptr_array(grads), a, ctypes.byref(layout.c), adam_, loss_scale, sum_mode,
                                    _ptr(state), _stream(stream)), "dp_step_single_pass")
+
+
+def dp_step_single_pass_from_host(replicas, master2, m2, v2, host_grads, grads, a: int, layout: Layout,
+                                  adam_: dp_adam_t, loss_scale: float, sum_mode: int = DP_SUM_COMPENSATED,
+                                  state=None, host_state=None, stream=None) -> None:
+    """dp_step_single_pass with the gradients in host memory (see dp_step_from_host for host_grads and
+    host_state)."""
+    lens = layout.shard_lens() * 2
+    for name, ts in (("master", master2), ("m", m2), ("v", v2)):
+        if len(ts) != 2 * layout.n:
+            raise ValueError("%s: need 2n = %d tensors" % (name, 2 * layout.n))
+        _check_tensors(ts, 4, lens, name)
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    _check_tensors(grads, 2, [layout.psi] * len(grads), "grads")
+    hp, hs = _host_args(layout, host_grads, grads, host_state)
+    _check(LIB.dp_step_single_pass_from_host(_ptr_array(replicas), _ptr_array(master2), _ptr_array(m2),
+                                             _ptr_array(v2), hp, _ptr_array(grads), a, ctypes.byref(layout.c), adam_,
+                                             loss_scale, sum_mode, _ptr(state), hs, _stream(stream)),
+           "dp_step_single_pass_from_host")
+
+
+def dp_commit_step(state, adam_: dp_adam_t, scaler_: Optional[dp_scaler_t] = None, stream=None) -> None:
+    """Commits a step reduced with DP_DEFER_COMMIT once found_inf holds every slice's decision."""
+    _check(LIB.dp_commit_step(_ptr(state), adam_, ctypes.byref(scaler_) if scaler_ is not None else None,
+                              _stream(stream)), "dp_commit_step")
+
+
+def dp_commit_single_pass(replicas, master2, layout: Layout, adam_: dp_adam_t, state,
+                          scaler_: Optional[dp_scaler_t] = None, stream=None) -> None:
+    """dp_commit_step for a single pass run with DP_DEFER_COMMIT: flips the state set unless skipped, and
+    repairs the replicas on a skipped step."""
+    if len(master2) != 2 * layout.n:
+        raise ValueError("master: need 2n = %d tensors" % (2 * layout.n))
+    _check_tensors(master2, 4, layout.shard_lens() * 2, "master")
+    _check_tensors(replicas, 2, [layout.psi] * layout.n, "replicas")
+    _check(LIB.dp_commit_single_pass(_ptr_array(replicas), _ptr_array(master2), ctypes.byref(layout.c), adam_,
+                                     ctypes.byref(scaler_) if scaler_ is not None else None, _ptr(state),
+                                     _stream(stream)), "dp_commit_single_pass")
 
 
 STATIC_SCRATCH_BYTES = 64 * 1024 * 1024

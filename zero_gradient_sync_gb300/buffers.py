@@ -58,6 +58,14 @@ class StepBuffers:
                                  self.grads, self.a, self.layout, adam_, loss_scale, sum_mode, state=self.state,
                                  stream=stream)
 
+    def step_single_pass_from_host(self, host_grads, adam_: _lib.dp_adam_t, loss_scale: float,
+                                   sum_mode: int = DP_SUM_COMPENSATED, host_state=None, stream=None) -> None:
+        """One single-pass step with this step's gradients in host memory (copied into self.grads first)."""
+        _lib.dp_step_single_pass_from_host(self.replicas, self.master + self.master1, self.m + self.m1,
+                                           self.v + self.v1, host_grads, self.grads, self.a, self.layout, adam_,
+                                           loss_scale, sum_mode, state=self.state, host_state=host_state,
+                                           stream=stream)
+
     def current(self):
         """The current (master, m, v) set of a single-pass run."""
         cur = _lib.read_state(self.state)["cur_set"]

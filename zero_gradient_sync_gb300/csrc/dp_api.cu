@@ -129,16 +129,41 @@ dp_status_t check_adam(const dp_adam_t& A) {
   return DP_OK;
 }
 
-// sum_mode = arithmetic (DP_SUM_*) | rank order (DP_ORDER_*).
-static bool split_mode(int sum_mode, int& arith, int& order) {
+// The scaler argument of a commit: NULL keeps the scale as it is.
+dp_status_t scaler_of(const dp_scaler_t* scaler, dp::ScalerK& k) {
+  k = dp::ScalerK{0, 1, 1.0f, 1.0f, 1.0f, 1.0f, 0};
+  if (!scaler) return DP_OK;
+  const dp_scaler_t& c = *scaler;
+  if (!(std::isfinite(c.growth_factor) && c.growth_factor >= 1.0f) ||
+      !(c.backoff_factor > 0.0f && c.backoff_factor <= 1.0f) || c.growth_interval < 1 ||
+      !(c.min_scale > 0.0f) || !std::isfinite(c.max_scale) || !(c.max_scale >= c.min_scale))
+    return fail(DP_ERR_INVALID_ARG, "scaler: need growth >= 1, backoff in (0, 1], interval >= 1, "
+                                    "0 < min_scale <= max_scale < inf");
+  k = dp::ScalerK{1, c.growth_interval, c.growth_factor, c.backoff_factor, c.min_scale, c.max_scale, 1};
+  return DP_OK;
+}
+
+// sum_mode = arithmetic (DP_SUM_*) | rank order (DP_ORDER_*) | step flags (DP_DEFER_COMMIT, DP_DEVICE_SCALE).
+constexpr int kFlagBits = DP_DEFER_COMMIT | DP_DEVICE_SCALE;
+static bool split_mode(int sum_mode, int& arith, int& order, int* flags = nullptr) {
   arith = sum_mode & 0xF;
-  order = sum_mode & ~0xF;
+  order = sum_mode & DP_ORDER_TREE;
+  const int f = sum_mode & kFlagBits;
+  if (flags) *flags = f;
+  else if (f) return false;
+  if (sum_mode & ~(0xF | DP_ORDER_TREE | kFlagBits)) return false;
   return (arith == DP_SUM_COMPENSATED || arith == DP_SUM_PLAIN) && (order == DP_ORDER_RING || order == DP_ORDER_TREE);
 }
 
-dp_status_t scalars(const Plan& P, const dp_adam_t* A, float loss_scale, int sum_mode, StepScalars& s) {
-  int arith = 0, order = 0;
-  if (!split_mode(sum_mode, arith, order)) return fail(DP_ERR_INVALID_ARG, "sum_mode %d unknown", sum_mode);
+// allowed: the step flags this entry point accepts.  With DP_DEVICE_SCALE the reduction unscales by the
+// device-resident scale (read and checked on the device) and loss_scale is not used.
+dp_status_t scalars(const Plan& P, const dp_adam_t* A, float loss_scale, int sum_mode, StepScalars& s,
+                    int allowed = 0) {
+  int arith = 0, order = 0, flags = 0;
+  if (!split_mode(sum_mode, arith, order, &flags)) return fail(DP_ERR_INVALID_ARG, "sum_mode %d unknown", sum_mode);
+  if (flags & ~allowed)
+    return fail(DP_ERR_INVALID_ARG, "sum_mode flag 0x%x is not accepted by this call", flags & ~allowed);
+  if (flags & DP_DEVICE_SCALE) loss_scale = 1.0f;
   if (!std::isfinite(loss_scale) || !(loss_scale > 0.0f))
     return fail(DP_ERR_INVALID_ARG, "loss scale must be finite and > 0");
   const double inv = 1.0 / ((double)P.n * (double)loss_scale);
@@ -149,7 +174,8 @@ dp_status_t scalars(const Plan& P, const dp_adam_t* A, float loss_scale, int sum
   s.mode = arith;
   s.order = order;
   s.timeout_ns = g_timeout_ns.load();
-  s.scaler = dp::ScalerK{0, 1, 1.0f, 1.0f, 1.0f, 1.0f};
+  s.scaler = dp::ScalerK{(flags & DP_DEVICE_SCALE) ? 1 : 0, 1, 1.0f, 1.0f, 1.0f, 1.0f, 0};
+  s.defer = (flags & DP_DEFER_COMMIT) ? 1 : 0;
   if (A) {
     dp_status_t st = check_adam(*A);
     if (st != DP_OK) return st;
@@ -260,6 +286,48 @@ dp_status_t dp_layout_even(int64_t psi, int32_t n, int64_t bucket, int32_t misal
       }
     }
   }
+  *nseg = count;
+  return DP_OK;
+}
+
+dp_status_t dp_layout_slice(const dp_layout_t* layout, int64_t lo, int64_t hi, dp_segment_t* out, int32_t* nseg,
+                            int64_t* local_base) {
+  static thread_local Plan P;
+  if (!nseg) return fail(DP_ERR_INVALID_ARG, "nseg is NULL");
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  if (lo < 0 || hi < lo || hi > layout->psi)
+    return fail(DP_ERR_INVALID_ARG, "slice [%lld, %lld) not inside [0, %lld)", (long long)lo, (long long)hi,
+                (long long)layout->psi);
+  // Pieces of the non-empty segments inside [lo, hi), and the lowest local index of each owner's pieces.
+  int64_t base[DP_MAX_N];
+  for (int r = 0; r < DP_MAX_N; ++r) base[r] = INT64_MAX;
+  int32_t count = 0;
+  for (int k = 0; k < P.nseg; ++k) {
+    const int64_t g0 = std::max(P.e[k].goff, lo), g1 = std::min(P.e[k + 1].goff, hi);
+    if (g0 >= g1) continue;
+    const int32_t o = P.e[k].owner;
+    base[o] = std::min(base[o], P.e[k].loff + (g0 - P.e[k].goff));
+    ++count;
+  }
+  for (int r = 0; r < P.n; ++r)
+    if (base[r] == INT64_MAX) base[r] = 0;   // no piece of this owner in the slice
+  if (out) {
+    if (*nseg < count) return fail(DP_ERR_INVALID_ARG, "capacity %d < %d segments", *nseg, count);
+    int32_t idx = 0;
+    for (int k = 0; k < P.nseg; ++k) {
+      const int64_t g0 = std::max(P.e[k].goff, lo), g1 = std::min(P.e[k + 1].goff, hi);
+      if (g0 >= g1) continue;
+      dp_segment_t& e = out[idx++];
+      e.global_off = g0 - lo;
+      e.len = g1 - g0;
+      e.owner = P.e[k].owner;
+      e.reserved = 0;
+      e.local_off = P.e[k].loff + (g0 - P.e[k].goff) - base[e.owner];
+    }
+  }
+  if (local_base)
+    for (int r = 0; r < P.n; ++r) local_base[r] = base[r];
   *nseg = count;
   return DP_OK;
 }
@@ -415,10 +483,10 @@ dp_status_t dp_allgather_params(uint16_t* const* replicas, const float* const* m
 
 static dp_status_t prepare_reduce(const Plan& P, const uint16_t* const* grads, int32_t a, const dp_adam_t& adam,
                                   float loss_scale, int32_t sum_mode, float* const* gbar_shard, void* ws,
-                                  dp_step_state_t* d_state, StepScalars& s, float** gb) {
+                                  dp_step_state_t* d_state, StepScalars& s, float** gb, int allowed = 0) {
   if (a < 1 || (int64_t)a * P.n > DP_MAX_NA)
     return fail(DP_ERR_INVALID_ARG, "a = %d: need 1 <= a and n * a <= %d", a, DP_MAX_NA);
-  dp_status_t st = scalars(P, &adam, loss_scale, sum_mode, s);
+  dp_status_t st = scalars(P, &adam, loss_scale, sum_mode, s, allowed);
   if (st == DP_OK) st = check_full_arrays(P, (const void* const*)grads, P.n * a, "grads");
   if (st == DP_OK) st = gbar_ptrs(P, gbar_shard, ws, gb);
   if (st == DP_OK) st = check_state(d_state);
@@ -430,8 +498,9 @@ static dp_status_t prepare_reduce(const Plan& P, const uint16_t* const* grads, i
 static cudaError_t launch_pass_a(const Plan& P, const uint16_t* const* grads, int a, float* const* gb,
                                  const StepScalars& s, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
   dp::NvtxRange range("dpstep pass A: accumulate, reduce-scatter, average, check");
-  if (s.order == DP_ORDER_TREE) return dp::launch_reduce_tree(P, grads, a, gb, s, 1, st, stream, launches);
-  return dp::launch_reduce(P, grads, a, gb, s, 1, st, stream, launches);
+  const int advance = s.defer ? 0 : 1;
+  if (s.order == DP_ORDER_TREE) return dp::launch_reduce_tree(P, grads, a, gb, s, advance, st, stream, launches);
+  return dp::launch_reduce(P, grads, a, gb, s, advance, st, stream, launches);
 }
 
 static cudaError_t launch_pass_b(const Plan& P, uint16_t* const* rep, float* const* master, float* const* m,
@@ -449,7 +518,8 @@ dp_status_t dp_step_reduce(float* const* gbar_shard, void* ws, const uint16_t* c
   if (st != DP_OK) return st;
   StepScalars s;
   float* gb[DP_MAX_N];
-  if ((st = prepare_reduce(P, grads, a, adam, loss_scale, sum_mode, gbar_shard, ws, d_state, s, gb)) != DP_OK)
+  if ((st = prepare_reduce(P, grads, a, adam, loss_scale, sum_mode, gbar_shard, ws, d_state, s, gb,
+                           DP_DEFER_COMMIT | DP_DEVICE_SCALE)) != DP_OK)
     return st;
   LaunchCount lc;
   cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, (cudaStream_t)stream, &lc.n);
@@ -465,7 +535,7 @@ dp_status_t dp_reduce_scatter_micro(float* const* acc_shard, float* const* gbar_
   if (st != DP_OK) return st;
   if (a < 1 || k < 0 || k >= a) return fail(DP_ERR_INVALID_ARG, "micro-step k = %d of a = %d", k, a);
   StepScalars s;
-  if ((st = scalars(P, &adam, loss_scale, sum_mode, s)) != DP_OK) return st;
+  if ((st = scalars(P, &adam, loss_scale, sum_mode, s, DP_DEFER_COMMIT | DP_DEVICE_SCALE)) != DP_OK) return st;
   if (s.order != DP_ORDER_RING) return fail(DP_ERR_INVALID_ARG, "dp_reduce_scatter_micro: ring order only");
   if ((st = check_full_arrays(P, (const void* const*)g, P.n, "g")) != DP_OK) return st;
   if (a > 1) {
@@ -584,12 +654,8 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
   dp_status_t st = build_plan(layout, P);
   if (st != DP_OK) return st;
   if (!scaler) return fail(DP_ERR_INVALID_ARG, "scaler is NULL");
-  const dp_scaler_t& c = *scaler;
-  if (!(std::isfinite(c.growth_factor) && c.growth_factor >= 1.0f) ||
-      !(c.backoff_factor > 0.0f && c.backoff_factor <= 1.0f) || c.growth_interval < 1 ||
-      !(c.min_scale > 0.0f) || !std::isfinite(c.max_scale) || !(c.max_scale >= c.min_scale))
-    return fail(DP_ERR_INVALID_ARG, "scaler: need growth >= 1, backoff in (0, 1], interval >= 1, "
-                                    "0 < min_scale <= max_scale < inf");
+  dp::ScalerK k;
+  if ((st = scaler_of(scaler, k)) != DP_OK) return st;
   StepScalars s;
   float* gb[DP_MAX_N];
   // The fixed-scale checks run with scale 1; the real scale is read and checked on the device.
@@ -597,7 +663,7 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
     return st;
   if ((st = check_state_arrays(P, master, m, v)) != DP_OK) return st;
   if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
-  s.scaler = dp::ScalerK{1, c.growth_interval, c.growth_factor, c.backoff_factor, c.min_scale, c.max_scale};
+  s.scaler = k;
   LaunchCount lc;
   cudaError_t e = launch_pass_a(P, grads, a, gb, s, d_state, (cudaStream_t)stream, &lc.n);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
@@ -605,9 +671,16 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "update launch");
 }
 
-dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
-                                const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
-                                float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// dp_step_single_pass, optionally preceded by the host-to-device copies of its gradients and followed by the
+// copy of its state to the host (dp_step_single_pass_from_host).  Every argument is checked first.
+dp_status_t single_pass_impl(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                             const uint16_t* const* host_grads, const uint16_t* const* grads, int32_t a,
+                             const dp_layout_t* layout, dp_adam_t adam, float loss_scale, int32_t sum_mode,
+                             dp_step_state_t* d_state, dp_step_state_t* host_state, cudaStream_t stream) {
   static thread_local Plan P;
   dp_status_t st = build_plan(layout, P);
   if (st != DP_OK) return st;
@@ -615,7 +688,7 @@ dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master,
   if (a < 1 || (int64_t)a * P.n > DP_MAX_NA)
     return fail(DP_ERR_INVALID_ARG, "a = %d: need 1 <= a and n * a <= %d", a, DP_MAX_NA);
   StepScalars s;
-  if ((st = scalars(P, &adam, loss_scale, sum_mode, s)) != DP_OK) return st;
+  if ((st = scalars(P, &adam, loss_scale, sum_mode, s, DP_DEFER_COMMIT | DP_DEVICE_SCALE)) != DP_OK) return st;
   if (s.order != DP_ORDER_RING) return fail(DP_ERR_INVALID_ARG, "dp_step_single_pass: ring order only");
   if ((st = check_full_arrays(P, (const void* const*)grads, P.n * a, "grads")) != DP_OK) return st;
   if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
@@ -625,11 +698,88 @@ dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master,
   if ((st = check_ptr_array((const void* const*)m, 2 * P.n, "m (2 sets)", lens2)) != DP_OK) return st;
   if ((st = check_ptr_array((const void* const*)v, 2 * P.n, "v (2 sets)", lens2)) != DP_OK) return st;
   if ((st = check_state(d_state)) != DP_OK) return st;
+  if (host_grads &&
+      (st = check_full_arrays(P, (const void* const*)host_grads, P.n * a, "host_grads")) != DP_OK)
+    return st;
+  const size_t bytes = (size_t)P.psi * sizeof(uint16_t);
+  if (host_grads && bytes) {
+    dp::NvtxRange range("dpstep gradient copies to the device");
+    for (int q = 0; q < P.n * a; ++q) {
+      const cudaError_t e = cudaMemcpyAsync(const_cast<uint16_t*>(grads[q]), host_grads[q], bytes,
+                                            cudaMemcpyHostToDevice, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "gradient copy to the device");
+    }
+  }
   LaunchCount lc;
-  dp::NvtxRange range("dpstep single pass: reduce, adam, all-gather");
-  cudaError_t e = dp::launch_single_pass(P, grads, a, replicas, master, m, v, s, d_state, (cudaStream_t)stream,
-                                         &lc.n);
-  return e == cudaSuccess ? DP_OK : cuda_fail(e, "single-pass launch");
+  {
+    dp::NvtxRange range("dpstep single pass: reduce, adam, all-gather");
+    cudaError_t e = dp::launch_single_pass(P, grads, a, replicas, master, m, v, s, d_state, stream, &lc.n);
+    if (e != cudaSuccess) return cuda_fail(e, "single-pass launch");
+  }
+  if (host_state) {
+    const cudaError_t e = cudaMemcpyAsync(host_state, d_state, sizeof(dp_step_state_t), cudaMemcpyDeviceToHost,
+                                          stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy to the host");
+  }
+  return DP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dp_status_t dp_step_single_pass(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
+                                const uint16_t* const* grads, int32_t a, const dp_layout_t* layout, dp_adam_t adam,
+                                float loss_scale, int32_t sum_mode, dp_step_state_t* d_state, dp_stream_t stream) {
+  return single_pass_impl(replicas, master, m, v, nullptr, grads, a, layout, adam, loss_scale, sum_mode, d_state,
+                          nullptr, (cudaStream_t)stream);
+}
+
+dp_status_t dp_step_single_pass_from_host(uint16_t* const* replicas, float* const* master, float* const* m,
+                                          float* const* v, const uint16_t* const* host_grads, uint16_t* const* grads,
+                                          int32_t a, const dp_layout_t* layout, dp_adam_t adam, float loss_scale,
+                                          int32_t sum_mode, dp_step_state_t* d_state, dp_step_state_t* host_state,
+                                          dp_stream_t stream) {
+  if (!host_grads) return fail(DP_ERR_INVALID_ARG, "dp_step_single_pass_from_host: host_grads is NULL");
+  return single_pass_impl(replicas, master, m, v, host_grads, (const uint16_t* const*)grads, a, layout, adam,
+                          loss_scale, sum_mode, d_state, host_state, (cudaStream_t)stream);
+}
+
+dp_status_t dp_commit_step(dp_step_state_t* d_state, dp_adam_t adam, const dp_scaler_t* scaler, dp_stream_t stream) {
+  dp_status_t st = check_state(d_state);
+  if (st != DP_OK) return st;
+  if ((st = check_adam(adam)) != DP_OK) return st;
+  dp::ScalerK k;
+  if ((st = scaler_of(scaler, k)) != DP_OK) return st;
+  LaunchCount lc;
+  dp::NvtxRange range("dpstep commit");
+  cudaError_t e = dp::launch_commit(d_state, (double)adam.beta1, (double)adam.beta2, k, 0, (cudaStream_t)stream,
+                                    &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "commit launch");
+}
+
+dp_status_t dp_commit_single_pass(uint16_t* const* replicas, float* const* master, const dp_layout_t* layout,
+                                  dp_adam_t adam, const dp_scaler_t* scaler, dp_step_state_t* d_state,
+                                  dp_stream_t stream) {
+  static thread_local Plan P;
+  dp_status_t st = build_plan(layout, P);
+  if (st != DP_OK) return st;
+  if (P.stage == 0) return fail(DP_ERR_INVALID_ARG, "dp_commit_single_pass: stage 0 is not supported");
+  if ((st = check_state(d_state)) != DP_OK) return st;
+  if ((st = check_adam(adam)) != DP_OK) return st;
+  if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
+  int64_t lens2[2 * DP_MAX_N];
+  for (int r = 0; r < P.n; ++r) lens2[r] = lens2[P.n + r] = P.shard_len[r];
+  if ((st = check_ptr_array((const void* const*)master, 2 * P.n, "master (2 sets)", lens2)) != DP_OK) return st;
+  dp::ScalerK k;
+  if ((st = scaler_of(scaler, k)) != DP_OK) return st;
+  LaunchCount lc;
+  dp::NvtxRange range("dpstep commit (single pass)");
+  cudaError_t e = dp::launch_commit(d_state, (double)adam.beta1, (double)adam.beta2, k, 1, (cudaStream_t)stream,
+                                    &lc.n);
+  if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+  e = dp::launch_repair(P, replicas, master, d_state, (cudaStream_t)stream, &lc.n);
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "repair launch");
 }
 
 dp_status_t dp_read_status(const dp_step_state_t* d_state, int32_t* skipped, int32_t* err, dp_stream_t stream) {

@@ -256,16 +256,44 @@ __device__ __forceinline__ void record_error(dp_step_state_t* st, int code) {
   atomicCAS(&st->error, 0, code);
 }
 
-// End of a reduction kernel, run by thread 0 of every CTA: fold the CTA's
-// non-finite count into the state; the last CTA to arrive publishes
-// found_inf / nonfinite, optionally advances t and the beta powers, and
-// clears the work fields for the next call.
-// Dynamic loss-scale policy applied by the last CTA of a reduction (see dp_scaler_t).
+// Dynamic loss-scale policy applied when a step is committed (see dp_scaler_t).
 struct ScalerK {
-  int32_t enabled, interval;
+  int32_t enabled;   // the reduction unscales by the device-resident scale
+  int32_t interval;
   float growth, backoff, min_scale, max_scale;
+  int32_t update;    // the commit applies the policy to the device-resident scale
 };
 
+// Commits a step once its skip decision `found` is final: unless found, t and the beta powers advance (and the
+// single pass's current state set flips); the dynamic loss scale follows the decision unless a device error
+// stopped the step.  Run by one thread.
+__device__ __forceinline__ void commit_state(dp_step_state_t* st, int found, int err, double b1, double b2,
+                                             const ScalerK* scaler, int flip_set) {
+  if (!found) {
+    st->t += 1;
+    st->b1t *= b1;
+    st->b2t *= b2;
+    if (flip_set) st->cur_set ^= 1u;
+  }
+  if (scaler && scaler->update && err == 0) {
+    float sc = st->loss_scale;
+    if (found) {
+      sc = fmaxf(__fmul_rn(sc, scaler->backoff), scaler->min_scale);
+      st->good_steps = 0;
+    } else if (st->good_steps + 1 >= scaler->interval) {
+      sc = fminf(__fmul_rn(sc, scaler->growth), scaler->max_scale);
+      st->good_steps = 0;
+    } else {
+      st->good_steps += 1;
+    }
+    st->loss_scale = sc;
+  }
+}
+
+// End of a reduction kernel, run by thread 0 of every CTA: fold the CTA's non-finite count into the state; the
+// last CTA to arrive publishes found_inf / nonfinite, commits the step unless the commit is deferred (advance
+// = 0: the caller first combines found_inf across slices, then commits), and clears the work fields for the
+// next call.
 __device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned long long cta_count, int cta_found,
                                                  int advance, double b1, double b2,
                                                  const ScalerK* scaler = nullptr, int flip_set = 0) {
@@ -281,25 +309,7 @@ __device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned l
     const int found = (f != 0u || err != 0) ? 1 : 0;
     st->found_inf = found;
     st->nonfinite = c;
-    if (advance && !found) {
-      st->t += 1;
-      st->b1t *= b1;
-      st->b2t *= b2;
-      if (flip_set) st->cur_set ^= 1u;
-    }
-    if (scaler && scaler->enabled && err == 0) {
-      float sc = st->loss_scale;
-      if (found) {
-        sc = fmaxf(__fmul_rn(sc, scaler->backoff), scaler->min_scale);
-        st->good_steps = 0;
-      } else if (st->good_steps + 1 >= scaler->interval) {
-        sc = fminf(__fmul_rn(sc, scaler->growth), scaler->max_scale);
-        st->good_steps = 0;
-      } else {
-        st->good_steps += 1;
-      }
-      st->loss_scale = sc;
-    }
+    if (advance) commit_state(st, found, err, b1, b2, scaler, flip_set);
     __threadfence();
     atomicExch(&st->work_ticket, 0u);
   }

@@ -30,6 +30,7 @@ struct StepScalars {
   int32_t order;  // DP_ORDER_RING or DP_ORDER_TREE
   uint64_t timeout_ns;
   ScalerK scaler;  // disabled unless the step uses the device-resident loss scale
+  int32_t defer;   // DP_DEFER_COMMIT: the reduction publishes found_inf only; dp_commit_* commits later
 };
 
 // A named range on the host timeline around the launches of one phase of the step (pass A, pass B, ...), so a
@@ -71,6 +72,11 @@ cudaError_t launch_advance(dp_step_state_t* st, double b1, double b2, cudaStream
 cudaError_t launch_allgather(const Plan& P, uint16_t* const* rep, const float* const* master,
                              const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
 cudaError_t launch_state_init(dp_step_state_t* st, cudaStream_t stream, uint64_t* launches);
+// Deferred commit (one thread) and the single pass's replica repair (work only on a skipped step).
+cudaError_t launch_commit(dp_step_state_t* st, double b1, double b2, const ScalerK& scaler, int flip_set,
+                          cudaStream_t stream, uint64_t* launches);
+cudaError_t launch_repair(const Plan& P, uint16_t* const* rep, float* const* master2, const dp_step_state_t* st,
+                          cudaStream_t stream, uint64_t* launches);
 cudaError_t launch_scaler_init(dp_step_state_t* st, float scale, cudaStream_t stream, uint64_t* launches);
 cudaError_t launch_selftest_wait(dp_step_state_t* st, uint64_t timeout_ns, cudaStream_t stream, uint64_t* launches);
 

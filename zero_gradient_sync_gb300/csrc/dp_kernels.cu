@@ -934,6 +934,15 @@ __global__ void advance_kernel(dp_step_state_t* st, double b1, double b2) {
   }
 }
 
+// The commit of a step whose reduction deferred it: found_inf now holds the decision of every slice (a
+// recorded device error also skips the step).
+__global__ void commit_kernel(dp_step_state_t* st, double b1, double b2, ScalerK scaler, int flip_set) {
+  const int err = st->error;
+  const int found = (st->found_inf != 0 || err != 0) ? 1 : 0;
+  st->found_inf = found;
+  commit_state(st, found, err, b1, b2, &scaler, flip_set);
+}
+
 __global__ void state_init_kernel(dp_step_state_t* st) {
   st->t = 0;
   st->found_inf = 0;
@@ -1070,24 +1079,13 @@ __global__ void __launch_bounds__(256) repair_kernel(const __grid_constant__ Rep
 }
 
 template <int MAXSEG>
-static cudaError_t launch_single_t(const Plan& P, const uint16_t* const* g, int a, const StepScalars& s,
-                                   dp_step_state_t* st, const FusedArgs& fa, cudaStream_t stream) {
-  // gbar stays in registers when every shard offset keeps 4-groups aligned and a tile has enough inputs for the
-  // fourth stage to pay; otherwise the shared gbar tile regroups it.
-  bool realign = P.n * a >= 16;
-  for (int k = 0; k < P.nseg; ++k)
-    if (((P.e[k].loff - P.e[k].goff) & 3) != 0) realign = false;
-  const bool comp = s.mode == DP_SUM_COMPENSATED;
-  cudaError_t e = realign ? (comp ? launch_reduce_t<MAXSEG, true, 2>(P, g, a, nullptr, s, 1, st, &fa, stream)
-                                  : launch_reduce_t<MAXSEG, false, 2>(P, g, a, nullptr, s, 1, st, &fa, stream))
-                          : (comp ? launch_reduce_t<MAXSEG, true, 1>(P, g, a, nullptr, s, 1, st, &fa, stream)
-                                  : launch_reduce_t<MAXSEG, false, 1>(P, g, a, nullptr, s, 1, st, &fa, stream));
-  if (e != cudaSuccess) return e;
+static cudaError_t launch_repair_t(const Plan& P, uint16_t* const* rep, float* const* master2,
+                                   const dp_step_state_t* st, cudaStream_t stream) {
   RepairParams<MAXSEG> rp;
   for (int r = 0; r < P.n; ++r) {
-    rp.rep[r] = fa.rep[r];
-    rp.master[0][r] = fa.master[r];
-    rp.master[1][r] = fa.master[P.n + r];
+    rp.rep[r] = rep[r];
+    rp.master[0][r] = master2[r];
+    rp.master[1][r] = master2[P.n + r];
   }
   rp.state = st;
   rp.n = P.n;
@@ -1097,10 +1095,28 @@ static cudaError_t launch_single_t(const Plan& P, const uint16_t* const* g, int 
   return cudaGetLastError();
 }
 
+template <int MAXSEG>
+static cudaError_t launch_single_t(const Plan& P, const uint16_t* const* g, int a, const StepScalars& s,
+                                   dp_step_state_t* st, const FusedArgs& fa, cudaStream_t stream) {
+  // gbar stays in registers when every shard offset keeps 4-groups aligned and a tile has enough inputs for the
+  // fourth stage to pay; otherwise the shared gbar tile regroups it.
+  bool realign = P.n * a >= 16;
+  for (int k = 0; k < P.nseg; ++k)
+    if (((P.e[k].loff - P.e[k].goff) & 3) != 0) realign = false;
+  const bool comp = s.mode == DP_SUM_COMPENSATED;
+  const int adv = s.defer ? 0 : 1;
+  cudaError_t e = realign ? (comp ? launch_reduce_t<MAXSEG, true, 2>(P, g, a, nullptr, s, adv, st, &fa, stream)
+                                  : launch_reduce_t<MAXSEG, false, 2>(P, g, a, nullptr, s, adv, st, &fa, stream))
+                          : (comp ? launch_reduce_t<MAXSEG, true, 1>(P, g, a, nullptr, s, adv, st, &fa, stream)
+                                  : launch_reduce_t<MAXSEG, false, 1>(P, g, a, nullptr, s, adv, st, &fa, stream));
+  if (e != cudaSuccess || s.defer) return e;   // deferred: the commit call launches the repair
+  return launch_repair_t<MAXSEG>(P, fa.rep, fa.master, st, stream);
+}
+
 cudaError_t launch_single_pass(const Plan& P, const uint16_t* const* g, int a, uint16_t* const* rep,
                                float* const* master2, float* const* m2, float* const* v2, const StepScalars& s,
                                dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
-  *launches += 2;
+  *launches += s.defer ? 1 : 2;
   const FusedArgs fa{master2, m2, v2, rep};
   if (P.nseg <= SMALL_SEG) return launch_single_t<SMALL_SEG>(P, g, a, s, st, fa, stream);
   return launch_single_t<BIG_SEG>(P, g, a, s, st, fa, stream);
@@ -1236,6 +1252,20 @@ cudaError_t launch_allgather(const Plan& P, uint16_t* const* rep, const float* c
   ++*launches;
   if (P.nseg <= SMALL_SEG) return launch_ag_t<SMALL_SEG>(P, rep, master, st, stream);
   return launch_ag_t<BIG_SEG>(P, rep, master, st, stream);
+}
+
+cudaError_t launch_repair(const Plan& P, uint16_t* const* rep, float* const* master2, const dp_step_state_t* st,
+                          cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  if (P.nseg <= SMALL_SEG) return launch_repair_t<SMALL_SEG>(P, rep, master2, st, stream);
+  return launch_repair_t<BIG_SEG>(P, rep, master2, st, stream);
+}
+
+cudaError_t launch_commit(dp_step_state_t* st, double b1, double b2, const ScalerK& scaler, int flip_set,
+                          cudaStream_t stream, uint64_t* launches) {
+  ++*launches;
+  commit_kernel<<<1, 1, 0, stream>>>(st, b1, b2, scaler, flip_set);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_state_init(dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {

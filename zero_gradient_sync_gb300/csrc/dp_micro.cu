@@ -38,7 +38,8 @@ struct MicroParams {
   double beta1, beta2;
   float inv;
   int32_t n;
-  ScalerK scaler;   // enabled (last launch only): unscale by the device-resident scale, then update it
+  int32_t advance;  // last launch: commit the step (0 when the commit is deferred)
+  ScalerK scaler;   // enabled (last launch only): unscale by the device-resident scale
   SegTable<MAXSEG> seg;
 };
 
@@ -228,7 +229,8 @@ __global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_const
     if ((threadIdx.x & 31) == 0 && c) atomicAdd(&s_count, c);
     __syncthreads();
     if (threadIdx.x == 0)
-      finish_reduction(p.state, s_count, (s_count != 0ull) || s_bad_scale, 1, p.beta1, p.beta2, &p.scaler, 0);
+      finish_reduction(p.state, s_count, (s_count != 0ull) || s_bad_scale, p.advance, p.beta1, p.beta2, &p.scaler,
+                       0);
   }
 }
 
@@ -246,6 +248,7 @@ cudaError_t launch_micro_t(const Plan& P, const uint16_t* const* g, float* const
   prm.beta2 = (double)s.beta2;
   prm.inv = s.inv;
   prm.n = P.n;
+  prm.advance = s.defer ? 0 : 1;
   prm.scaler = s.scaler;
   fill_seg(prm.seg, P);
   auto kern = rs_micro_kernel<MAXSEG, COMP, FLAGS>;
