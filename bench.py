@@ -64,9 +64,11 @@ def parse():
                    help="dp_step_single_pass (one pass, two state sets; the default), dp_step (reduce + update "
                         "kernels; the default with --order tree) or dp_reduce_scatter_micro per micro-step + "
                         "dp_step_update (the ZeRO-2 form)")
+    p.add_argument("--stage", type=int, default=-1, choices=[-1, 0, 1, 2, 3],
+                   help="override the workload's ZeRO stage (0: plain data parallelism, two-pass path)")
     args = p.parse_args()
     if args.path is None:
-        args.path = "two-pass" if args.order == "tree" else "single-pass"
+        args.path = "two-pass" if args.order == "tree" or args.stage == 0 else "single-pass"
     return args
 
 
@@ -111,7 +113,12 @@ def measured_peak():
 
 def step_bytes(wl):
     """Algorithmic bytes per parameter: single-pass minimum B1 = 2na + 24 + 2n; the two-pass design adds the
-    fp32 gbar shard written by the reduce kernel and read back by the update kernel (B2 = B1 + 8)."""
+    fp32 gbar shard written by the reduce kernel and read back by the update kernel (B2 = B1 + 8).  Plain data
+    parallelism (stage 0) keeps n full copies of master/m/v, so its update reads gbar once and reads and writes
+    every rank's state: B1 = 2na + 26n."""
+    if wl.stage == 0:
+        b1 = 2 * wl.n * wl.a + 26 * wl.n
+        return b1, b1 + 8, 2 * wl.n * wl.a + 4, 4 + 26 * wl.n
     b1 = 2 * wl.n * wl.a + 24 + 2 * wl.n
     return b1, b1 + 8, 2 * wl.n * wl.a + 4, 4 + 24 + 2 * wl.n
 
@@ -676,6 +683,8 @@ def main():
     wl = known[args.workload]
     if args.psi > 0:
         wl = wl.with_(psi=args.psi, description=wl.description + " [psi overridden to %d]" % args.psi)
+    if args.stage >= 0 and args.stage != wl.stage:
+        wl = wl.with_(stage=args.stage, description=wl.description + " [ZeRO stage overridden to %d]" % args.stage)
     if args.impl == "reference":
         return reference_main(args, wl)
     if args.checkpoint:

@@ -786,23 +786,81 @@ __global__ void __launch_bounds__(UB_THREADS) update_kernel(const __grid_constan
   if (REPL && tid == 0) bulk_wait_all();
 }
 
-// Stage 0 (plain data parallelism): every rank updates its own full-length
-// state with the owner's gbar, and writes its own replica.
+// Stage 0 (plain data parallelism): every rank updates its own full-length state with the owner's gbar, and
+// writes its own replica.  The work items of a tile are (rank, 4-element group) pairs of its 4-aligned global
+// interior, rank-major so that a warp's items are consecutive groups of one rank: each item reads the group's
+// master, m, v as 16-byte vectors at global index, writes them back and stores its four bf16 as one 8-byte
+// word.  The n items of a group read the same gbar vector (the tile's gbar, 30 KB, is served by L1/L2 after
+// the first).  UB_GROUPS items per thread have their loads issued before any arithmetic.  The <= 3 elements at
+// each end of the tile are updated one by one.
 template <int MAXSEG, bool REPL>
 __global__ void __launch_bounds__(UB_THREADS) update_dp_kernel(const __grid_constant__ UpdateParams<MAXSEG> p) {
   __shared__ float s_k[2];
   AdamK K;
   K.b1 = p.beta1; K.b2 = p.beta2; K.omb1 = p.omb1; K.omb2 = p.omb2; K.eps = p.eps;
   if (!update_prologue(p.state, p.lr, K, s_k)) return;
+  const int tid = threadIdx.x, n = p.n;
   const int ntiles = p.seg.ntiles;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const Tile t = tile_at(p.seg, tile);
-    const float* G = p.gbar[t.owner];
-    for (int64_t e = t.start + threadIdx.x; e < t.end; e += UB_THREADS) {
-      const float g = G[t.loff + (e - t.goff)];
-      for (int r = 0; r < p.n; ++r) {
+    const float* __restrict__ G = p.gbar[t.owner];
+    const int64_t delta = t.loff - t.goff;            // gbar's local index = global index + delta
+    const bool galign = (delta & 3) == 0;
+    const int64_t elo = (t.start + 3) & ~int64_t(3), ehi = t.end & ~int64_t(3);
+    const int ngr = ehi > elo ? (int)((ehi - elo) >> 2) : 0;
+    const int items = ngr * n;
+    for (int base = 0; base < items; base += UB_GROUPS * UB_THREADS) {
+      float4 g4[UB_GROUPS], t4[UB_GROUPS], m4[UB_GROUPS], v4[UB_GROUPS];
+      int rr[UB_GROUPS];
+      int64_t ee[UB_GROUPS];
+#pragma unroll
+      for (int u = 0; u < UB_GROUPS; ++u) {
+        const int w = base + tid + u * UB_THREADS;
+        rr[u] = -1;
+        if (w < items) {
+          const int r = w / ngr;
+          const int64_t e = elo + 4 * (int64_t)(w - r * ngr);
+          rr[u] = r;
+          ee[u] = e;
+          const float* gs = G + (e + delta);
+          g4[u] = galign ? *reinterpret_cast<const float4*>(gs) : make_float4(gs[0], gs[1], gs[2], gs[3]);
+          t4[u] = __ldcs(reinterpret_cast<const float4*>(p.master[r] + e));
+          m4[u] = __ldcs(reinterpret_cast<const float4*>(p.m[r] + e));
+          v4[u] = __ldcs(reinterpret_cast<const float4*>(p.v[r] + e));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UB_GROUPS; ++u) {
+        if (rr[u] >= 0) {
+          const int r = rr[u];
+          const int64_t e = ee[u];
+          adam1(g4[u].x, t4[u].x, m4[u].x, v4[u].x, K);
+          adam1(g4[u].y, t4[u].y, m4[u].y, v4[u].y, K);
+          adam1(g4[u].z, t4[u].z, m4[u].z, v4[u].z, K);
+          adam1(g4[u].w, t4[u].w, m4[u].w, v4[u].w, K);
+          __stcs(reinterpret_cast<float4*>(p.master[r] + e), t4[u]);
+          __stcs(reinterpret_cast<float4*>(p.m[r] + e), m4[u]);
+          __stcs(reinterpret_cast<float4*>(p.v[r] + e), v4[u]);
+          if (REPL)
+            __stcs(reinterpret_cast<uint2*>(p.rep[r] + e),
+                   make_uint2(bf16x2_rn(t4[u].x, t4[u].y), bf16x2_rn(t4[u].z, t4[u].w)));
+        }
+      }
+    }
+    // Ragged ends (at most 3 elements each) of every rank: thread 8r + k, k < 4 the head, k >= 4 the tail.
+    if (tid < 8 * n) {
+      const int r = tid >> 3, k = tid & 7;
+      int64_t e = -1;
+      if (k < 4) {
+        e = t.start + k;
+        if (e >= (elo < t.end ? elo : t.end)) e = -1;
+      } else {
+        e = (ehi > elo ? ehi : elo) + (k - 4);
+        if (e >= t.end) e = -1;
+      }
+      if (e >= 0) {
         float th = p.master[r][e], mm = p.m[r][e], vv = p.v[r][e];
-        adam1(g, th, mm, vv, K);
+        adam1(G[e + delta], th, mm, vv, K);
         p.master[r][e] = th;
         p.m[r][e] = mm;
         p.v[r][e] = vv;

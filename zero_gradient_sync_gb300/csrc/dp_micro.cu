@@ -25,7 +25,7 @@ namespace {
 
 constexpr int RM_THREADS = 256;
 constexpr int RM_EPT = 8;
-constexpr int RM_BATCH = 4;   // ranks whose loads are issued together
+constexpr int RM_BATCH = 8;   // ranks whose loads are issued together
 
 enum { RM_FIRST = 1, RM_LAST = 2 };   // flags: no accumulator to read / write gbar and finish
 
@@ -53,7 +53,7 @@ __device__ __forceinline__ uint4 load_group(const uint16_t* src, int64_t e0, int
 }
 
 template <int MAXSEG, bool COMP, int FLAGS>
-__global__ void __launch_bounds__(RM_THREADS) rs_micro_kernel(const __grid_constant__ MicroParams<MAXSEG> p) {
+__global__ void __launch_bounds__(RM_THREADS, 3) rs_micro_kernel(const __grid_constant__ MicroParams<MAXSEG> p) {
   constexpr bool FIRST = (FLAGS & RM_FIRST) != 0, LAST = (FLAGS & RM_LAST) != 0;
   __shared__ unsigned long long s_count;
   __shared__ float s_inv;
