@@ -118,7 +118,10 @@ enum { DP_DEFER_COMMIT = 32, DP_DEVICE_SCALE = 64 };
 /* ZeRO stages of the layout. */
 enum { DP_STAGE_DP = 0, DP_STAGE_ZERO1 = 1, DP_STAGE_ZERO2 = 2, DP_STAGE_ZERO3 = 3 };
 
-enum { DP_MAX_N = 16, DP_MAX_NA = 64, DP_MAX_SEG = 1024 };
+/* Limits: replicas, inputs (n * a), segments of a layout.  A layout of more
+ * than DP_KERNEL_SEG segments runs each kernel as several launches over
+ * contiguous runs of DP_KERNEL_SEG segments (results unchanged). */
+enum { DP_MAX_N = 16, DP_MAX_NA = 64, DP_MAX_SEG = 1 << 20, DP_KERNEL_SEG = 1024 };
 
 /* One contiguous piece of the flat parameter space [0, psi) and where its
  * optimizer state lives: elements [global_off, global_off + len) are owned by

@@ -18,7 +18,7 @@ DP_OK, DP_ERR_INVALID_ARG, DP_ERR_ALIGNMENT, DP_ERR_CUDA, DP_ERR_TIMEOUT, DP_ERR
 DP_SUM_COMPENSATED, DP_SUM_PLAIN = 0, 1
 DP_ORDER_RING, DP_ORDER_TREE = 0, 16   # OR'd into sum_mode
 DP_DEFER_COMMIT, DP_DEVICE_SCALE = 32, 64   # step flags, OR'd into sum_mode
-DP_MAX_N, DP_MAX_NA, DP_MAX_SEG = 16, 64, 1024
+DP_MAX_N, DP_MAX_NA, DP_MAX_SEG, DP_KERNEL_SEG = 16, 64, 1 << 20, 1024
 STATE_BYTES = 64
 
 c_i32, c_i64, c_u64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p

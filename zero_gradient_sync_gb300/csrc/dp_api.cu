@@ -77,6 +77,7 @@ dp_status_t build_plan(const dp_layout_t* L, Plan& P) {
   };
   std::vector<LR> locals;
   locals.reserve(L->nseg);
+  P.e.resize((size_t)L->nseg + 1);
   int64_t g = 0;
   int k = 0;
   int64_t tiles = 0;
@@ -114,6 +115,7 @@ dp_status_t build_plan(const dp_layout_t* L, Plan& P) {
       return fail(DP_ERR_INVALID_ARG, "rank %d: local ranges overlap", locals[i].owner);
   P.nseg = k;
   P.ntiles = (int32_t)tiles;
+  P.e.resize((size_t)k + 1);
   P.e[k].goff = L->psi;
   P.e[k].loff = 0;
   P.e[k].owner = 0;
@@ -176,6 +178,7 @@ dp_status_t scalars(const Plan& P, const dp_adam_t* A, float loss_scale, int sum
   s.timeout_ns = g_timeout_ns.load();
   s.scaler = dp::ScalerK{(flags & DP_DEVICE_SCALE) ? 1 : 0, 1, 1.0f, 1.0f, 1.0f, 1.0f, 0};
   s.defer = (flags & DP_DEFER_COMMIT) ? 1 : 0;
+  s.merge = 0;
   if (A) {
     dp_status_t st = check_adam(*A);
     if (st != DP_OK) return st;

@@ -17,7 +17,7 @@ namespace dp {
 
 constexpr int TILE = 7680;          // elements per tile, multiple of 8 (15 KB of bf16: one bulk copy)
 constexpr int SMALL_SEG = 32;       // segment-table capacity of the small kernel variants
-constexpr int BIG_SEG = DP_MAX_SEG; // ... and of the large ones
+constexpr int BIG_SEG = DP_KERNEL_SEG; // ... and of the large ones (a larger layout runs as several launches)
 
 struct SegEntry {
   int64_t goff;   // first global element of the segment
@@ -291,12 +291,12 @@ __device__ __forceinline__ void commit_state(dp_step_state_t* st, int found, int
 }
 
 // End of a reduction kernel, run by thread 0 of every CTA: fold the CTA's non-finite count into the state; the
-// last CTA to arrive publishes found_inf / nonfinite, commits the step unless the commit is deferred (advance
-// = 0: the caller first combines found_inf across slices, then commits), and clears the work fields for the
-// next call.
+// last CTA to arrive publishes found_inf / nonfinite (merge: ORed and added into what an earlier launch of the
+// same reduction published), commits the step unless the commit is deferred (advance = 0: a later launch, or
+// the caller after combining found_inf across slices, commits), and clears the work fields for the next call.
 __device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned long long cta_count, int cta_found,
                                                  int advance, double b1, double b2,
-                                                 const ScalerK* scaler = nullptr, int flip_set = 0) {
+                                                 const ScalerK* scaler = nullptr, int flip_set = 0, int merge = 0) {
   if (cta_count) atomicAdd(reinterpret_cast<unsigned long long*>(&st->work_count), cta_count);
   if (cta_found) atomicOr(&st->work_found, 1u);
   __threadfence();
@@ -304,9 +304,13 @@ __device__ __forceinline__ void finish_reduction(dp_step_state_t* st, unsigned l
   if (ticket == gridDim.x - 1) {
     __threadfence();
     const unsigned f = atomicExch(&st->work_found, 0u);
-    const unsigned long long c = atomicExch(reinterpret_cast<unsigned long long*>(&st->work_count), 0ull);
+    unsigned long long c = atomicExch(reinterpret_cast<unsigned long long*>(&st->work_count), 0ull);
     const int err = *reinterpret_cast<volatile int*>(&st->error);
-    const int found = (f != 0u || err != 0) ? 1 : 0;
+    int found = (f != 0u || err != 0) ? 1 : 0;
+    if (merge) {   // a later launch of the same reduction (a layout run in several launches)
+      found |= *reinterpret_cast<volatile int*>(&st->found_inf) != 0 ? 1 : 0;
+      c += *reinterpret_cast<volatile unsigned long long*>(&st->nonfinite);
+    }
     st->found_inf = found;
     st->nonfinite = c;
     if (advance) commit_state(st, found, err, b1, b2, scaler, flip_set);

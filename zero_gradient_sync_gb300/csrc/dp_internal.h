@@ -5,6 +5,8 @@
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "dp_device.cuh"
 #include "dpstep.h"
 
@@ -20,7 +22,7 @@ struct Plan {
   int32_t n, stage, nseg, ntiles;
   int64_t psi;
   int64_t shard_len[DP_MAX_N];
-  PlanSeg e[DP_MAX_SEG + 1];  // e[nseg] = {psi, 0, ntiles, 0}
+  std::vector<PlanSeg> e;  // nseg + 1 entries; e[nseg] = {end of the last segment, 0, ntiles, 0}
 };
 
 struct StepScalars {
@@ -31,7 +33,52 @@ struct StepScalars {
   uint64_t timeout_ns;
   ScalerK scaler;  // disabled unless the step uses the device-resident loss scale
   int32_t defer;   // DP_DEFER_COMMIT: the reduction publishes found_inf only; dp_commit_* commits later
+  int32_t merge;   // a later launch of one reduction: its finish ORs into found_inf and adds to nonfinite
 };
+
+// Segments one launch takes in its by-value table.  A layout with more segments runs as several launches over
+// contiguous runs of at most this many segments -- contiguous ranges of the parameter space, whose elements
+// keep their global and local indices.  Reductions then publish the skip decision over all the launches: the
+// first launch's finish sets found_inf and nonfinite, later ones OR and add into them, and only the last one
+// commits.
+constexpr int KERNEL_SEG = DP_KERNEL_SEG;
+
+// The plan of segments [s0, s1) of P, tiles renumbered from 0 (psi, n, stage and shard lengths kept).
+inline void chunk_plan(const Plan& P, int s0, int s1, Plan& C) {
+  C.n = P.n;
+  C.stage = P.stage;
+  C.psi = P.psi;
+  for (int r = 0; r < DP_MAX_N; ++r) C.shard_len[r] = P.shard_len[r];
+  C.nseg = s1 - s0;
+  C.e.resize((size_t)C.nseg + 1);
+  const int32_t t0 = P.e[s0].tile0;
+  for (int k = s0; k <= s1; ++k) {
+    C.e[k - s0] = P.e[k];
+    C.e[k - s0].tile0 -= t0;
+  }
+  C.e[C.nseg].loff = 0;
+  C.e[C.nseg].owner = 0;
+  C.ntiles = C.e[C.nseg].tile0;
+}
+
+// f(plan, scalars, last) once for P itself, or once per chunk of at most KERNEL_SEG segments with the
+// scalars of that launch (merge on every chunk but the first, defer on every chunk but the last).
+template <typename F>
+cudaError_t for_each_chunk(const Plan& P, const StepScalars& s, F&& f) {
+  if (P.nseg <= KERNEL_SEG) return f(P, s, true);
+  static thread_local Plan C;
+  for (int s0 = 0; s0 < P.nseg; s0 += KERNEL_SEG) {
+    const int s1 = P.nseg - s0 < KERNEL_SEG ? P.nseg : s0 + KERNEL_SEG;
+    const bool last = s1 == P.nseg;
+    chunk_plan(P, s0, s1, C);
+    StepScalars sc = s;
+    sc.merge = s0 > 0 ? 1 : 0;
+    sc.defer = (s.defer || !last) ? 1 : 0;
+    const cudaError_t e = f(static_cast<const Plan&>(C), static_cast<const StepScalars&>(sc), last);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 // A named range on the host timeline around the launches of one phase of the step (pass A, pass B, ...), so a
 // trace splits a step into its phases; costs nothing unless a profiler is attached (NVTX v3, header-only).

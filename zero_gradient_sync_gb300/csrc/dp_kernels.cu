@@ -67,6 +67,7 @@ struct ReduceParams {
   double beta1, beta2;
   float inv;
   int32_t n, a, advance;
+  int32_t merge;     // a later launch of one reduction (see finish_reduction)
   ScalerK scaler;    // enabled: unscale by the device-resident scale, then update it
   // single pass only: the two optimizer-state sets, the replicas, Adam constants
   float* st_master[2][DP_MAX_N];
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
   if (FUSED && tid == 0) bulk_wait_all();   // the last tile's replica stores
   if (tid == 0)
     finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2, &p.scaler,
-                     FUSED ? 1 : 0);
+                     FUSED ? 1 : 0, p.merge);
 }
 
 // ============================================================================ update (pass B)
@@ -910,7 +911,7 @@ struct RsParams {
   float* gbar[DP_MAX_N];
   dp_step_state_t* state;
   float inv;
-  int32_t n;
+  int32_t n, merge;
   SegTable<MAXSEG> seg;
 };
 
@@ -955,7 +956,7 @@ __global__ void __launch_bounds__(256) rs_avg_kernel(const __grid_constant__ RsP
   for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
   if ((threadIdx.x & 31) == 0 && c) atomicAdd(&s_count, c);
   __syncthreads();
-  if (threadIdx.x == 0) finish_reduction(p.state, s_count, s_count != 0ull, 0, 1.0, 1.0);
+  if (threadIdx.x == 0) finish_reduction(p.state, s_count, s_count != 0ull, 0, 1.0, 1.0, nullptr, 0, p.merge);
 }
 
 template <int MAXSEG>
@@ -1063,6 +1064,7 @@ static cudaError_t launch_reduce_t(const Plan& P, const uint16_t* const* g, int 
   prm.n = P.n;
   prm.a = a;
   prm.advance = advance;
+  prm.merge = s.merge;
   prm.scaler = s.scaler;
   if (fa) {
     for (int r = 0; r < P.n; ++r) {
@@ -1100,15 +1102,19 @@ static cudaError_t launch_reduce_t(const Plan& P, const uint16_t* const* g, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_reduce(const Plan& P, const uint16_t* const* g, int a, float* const* gbar, const StepScalars& s,
-                          int advance, dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
-  ++*launches;
-  const bool comp = s.mode == DP_SUM_COMPENSATED;
-  if (P.nseg <= SMALL_SEG)
-    return comp ? launch_reduce_t<SMALL_SEG, true, 0>(P, g, a, gbar, s, advance, st, nullptr, stream)
-                : launch_reduce_t<SMALL_SEG, false, 0>(P, g, a, gbar, s, advance, st, nullptr, stream);
-  return comp ? launch_reduce_t<BIG_SEG, true, 0>(P, g, a, gbar, s, advance, st, nullptr, stream)
-              : launch_reduce_t<BIG_SEG, false, 0>(P, g, a, gbar, s, advance, st, nullptr, stream);
+cudaError_t launch_reduce(const Plan& P0, const uint16_t* const* g, int a, float* const* gbar,
+                          const StepScalars& s0, int advance0, dp_step_state_t* st, cudaStream_t stream,
+                          uint64_t* launches) {
+  return for_each_chunk(P0, s0, [&](const Plan& P, const StepScalars& s, bool last) {
+    ++*launches;
+    const int advance = (advance0 && last) ? 1 : 0;
+    const bool comp = s.mode == DP_SUM_COMPENSATED;
+    if (P.nseg <= SMALL_SEG)
+      return comp ? launch_reduce_t<SMALL_SEG, true, 0>(P, g, a, gbar, s, advance, st, nullptr, stream)
+                  : launch_reduce_t<SMALL_SEG, false, 0>(P, g, a, gbar, s, advance, st, nullptr, stream);
+    return comp ? launch_reduce_t<BIG_SEG, true, 0>(P, g, a, gbar, s, advance, st, nullptr, stream)
+                : launch_reduce_t<BIG_SEG, false, 0>(P, g, a, gbar, s, advance, st, nullptr, stream);
+  });
 }
 
 // After a single-pass step: if it was skipped, rewrite the replicas as bf16 of the current (unchanged) master.
@@ -1167,17 +1173,20 @@ static cudaError_t launch_single_t(const Plan& P, const uint16_t* const* g, int 
                                   : launch_reduce_t<MAXSEG, false, 2>(P, g, a, nullptr, s, adv, st, &fa, stream))
                           : (comp ? launch_reduce_t<MAXSEG, true, 1>(P, g, a, nullptr, s, adv, st, &fa, stream)
                                   : launch_reduce_t<MAXSEG, false, 1>(P, g, a, nullptr, s, adv, st, &fa, stream));
-  if (e != cudaSuccess || s.defer) return e;   // deferred: the commit call launches the repair
-  return launch_repair_t<MAXSEG>(P, fa.rep, fa.master, st, stream);
+  return e;
 }
 
-cudaError_t launch_single_pass(const Plan& P, const uint16_t* const* g, int a, uint16_t* const* rep,
-                               float* const* master2, float* const* m2, float* const* v2, const StepScalars& s,
+cudaError_t launch_single_pass(const Plan& P0, const uint16_t* const* g, int a, uint16_t* const* rep,
+                               float* const* master2, float* const* m2, float* const* v2, const StepScalars& s0,
                                dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
-  *launches += s.defer ? 1 : 2;
   const FusedArgs fa{master2, m2, v2, rep};
-  if (P.nseg <= SMALL_SEG) return launch_single_t<SMALL_SEG>(P, g, a, s, st, fa, stream);
-  return launch_single_t<BIG_SEG>(P, g, a, s, st, fa, stream);
+  cudaError_t e = for_each_chunk(P0, s0, [&](const Plan& P, const StepScalars& s, bool) {
+    ++*launches;
+    if (P.nseg <= SMALL_SEG) return launch_single_t<SMALL_SEG>(P, g, a, s, st, fa, stream);
+    return launch_single_t<BIG_SEG>(P, g, a, s, st, fa, stream);
+  });
+  if (e != cudaSuccess || s0.defer) return e;   // deferred: the commit call launches the repair
+  return launch_repair(P0, rep, master2, st, stream, launches);
 }
 
 template <int MAXSEG>
@@ -1222,12 +1231,14 @@ static cudaError_t launch_update_t(const Plan& P, uint16_t* const* rep, float* c
   return cudaGetLastError();
 }
 
-cudaError_t launch_update(const Plan& P, uint16_t* const* rep, float* const* master, float* const* m,
-                          float* const* v, const float* const* gbar, const StepScalars& s,
+cudaError_t launch_update(const Plan& P0, uint16_t* const* rep, float* const* master, float* const* m,
+                          float* const* v, const float* const* gbar, const StepScalars& s0,
                           const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
-  ++*launches;
-  if (P.nseg <= SMALL_SEG) return launch_update_t<SMALL_SEG>(P, rep, master, m, v, gbar, s, st, stream);
-  return launch_update_t<BIG_SEG>(P, rep, master, m, v, gbar, s, st, stream);
+  return for_each_chunk(P0, s0, [&](const Plan& P, const StepScalars& s, bool) {
+    ++*launches;
+    if (P.nseg <= SMALL_SEG) return launch_update_t<SMALL_SEG>(P, rep, master, m, v, gbar, s, st, stream);
+    return launch_update_t<BIG_SEG>(P, rep, master, m, v, gbar, s, st, stream);
+  });
 }
 
 cudaError_t launch_accumulate(float* const* acc, const uint16_t* const* g, int64_t psi, int n, int first, int mode,
@@ -1263,6 +1274,7 @@ static cudaError_t launch_rs_t(const Plan& P, const float* const* acc, float* co
   prm.state = st;
   prm.inv = s.inv;
   prm.n = P.n;
+  prm.merge = s.merge;
   fill_seg(prm.seg, P);
   const int nt = P.ntiles > 0 ? P.ntiles : 1;
   if (s.mode == DP_SUM_COMPENSATED) {
@@ -1275,11 +1287,13 @@ static cudaError_t launch_rs_t(const Plan& P, const float* const* acc, float* co
   return cudaGetLastError();
 }
 
-cudaError_t launch_rs_avg(const Plan& P, const float* const* acc, float* const* gbar, const StepScalars& s,
+cudaError_t launch_rs_avg(const Plan& P0, const float* const* acc, float* const* gbar, const StepScalars& s0,
                           dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
-  ++*launches;
-  if (P.nseg <= SMALL_SEG) return launch_rs_t<SMALL_SEG>(P, acc, gbar, s, st, stream);
-  return launch_rs_t<BIG_SEG>(P, acc, gbar, s, st, stream);
+  return for_each_chunk(P0, s0, [&](const Plan& P, const StepScalars& s, bool) {
+    ++*launches;
+    if (P.nseg <= SMALL_SEG) return launch_rs_t<SMALL_SEG>(P, acc, gbar, s, st, stream);
+    return launch_rs_t<BIG_SEG>(P, acc, gbar, s, st, stream);
+  });
 }
 
 cudaError_t launch_advance(dp_step_state_t* st, double b1, double b2, cudaStream_t stream, uint64_t* launches) {
@@ -1305,18 +1319,24 @@ static cudaError_t launch_ag_t(const Plan& P, uint16_t* const* rep, const float*
   return cudaGetLastError();
 }
 
-cudaError_t launch_allgather(const Plan& P, uint16_t* const* rep, const float* const* master,
+cudaError_t launch_allgather(const Plan& P0, uint16_t* const* rep, const float* const* master,
                              const dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
-  ++*launches;
-  if (P.nseg <= SMALL_SEG) return launch_ag_t<SMALL_SEG>(P, rep, master, st, stream);
-  return launch_ag_t<BIG_SEG>(P, rep, master, st, stream);
+  StepScalars s0{};
+  return for_each_chunk(P0, s0, [&](const Plan& P, const StepScalars&, bool) {
+    ++*launches;
+    if (P.nseg <= SMALL_SEG) return launch_ag_t<SMALL_SEG>(P, rep, master, st, stream);
+    return launch_ag_t<BIG_SEG>(P, rep, master, st, stream);
+  });
 }
 
-cudaError_t launch_repair(const Plan& P, uint16_t* const* rep, float* const* master2, const dp_step_state_t* st,
+cudaError_t launch_repair(const Plan& P0, uint16_t* const* rep, float* const* master2, const dp_step_state_t* st,
                           cudaStream_t stream, uint64_t* launches) {
-  ++*launches;
-  if (P.nseg <= SMALL_SEG) return launch_repair_t<SMALL_SEG>(P, rep, master2, st, stream);
-  return launch_repair_t<BIG_SEG>(P, rep, master2, st, stream);
+  StepScalars s0{};
+  return for_each_chunk(P0, s0, [&](const Plan& P, const StepScalars&, bool) {
+    ++*launches;
+    if (P.nseg <= SMALL_SEG) return launch_repair_t<SMALL_SEG>(P, rep, master2, st, stream);
+    return launch_repair_t<BIG_SEG>(P, rep, master2, st, stream);
+  });
 }
 
 cudaError_t launch_commit(dp_step_state_t* st, double b1, double b2, const ScalerK& scaler, int flip_set,

@@ -54,6 +54,7 @@ struct TreeParams {
   double beta1, beta2;
   float inv;
   int32_t n, a, advance;
+  int32_t merge;     // a later launch of one reduction (see finish_reduction)
   ScalerK scaler;
   SegTable<MAXSEG> seg;
 };
@@ -361,7 +362,8 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
   if (lane == 0 && c) atomicAdd(s_count, c);
   __syncthreads();
   if (tid == 0)
-    finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2, &p.scaler, 0);
+    finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2, &p.scaler, 0,
+                     p.merge);
 }
 
 // ---------------------------------------------------------------- staged: the tree over per-rank accumulators
@@ -372,7 +374,7 @@ struct RsTreeParams {
   float* gbar[DP_MAX_N];
   dp_step_state_t* state;
   float inv;
-  int32_t n;
+  int32_t n, merge;
   SegTable<MAXSEG> seg;
 };
 
@@ -441,7 +443,7 @@ __global__ void __launch_bounds__(256) rs_tree_kernel(const __grid_constant__ Rs
   for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
   if ((threadIdx.x & 31) == 0 && c) atomicAdd(&s_count, c);
   __syncthreads();
-  if (threadIdx.x == 0) finish_reduction(p.state, s_count, s_count != 0ull, 0, 1.0, 1.0);
+  if (threadIdx.x == 0) finish_reduction(p.state, s_count, s_count != 0ull, 0, 1.0, 1.0, nullptr, 0, p.merge);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -460,6 +462,7 @@ cudaError_t launch_tree_t(const Plan& P, const uint16_t* const* g, int a, float*
   prm.n = P.n;
   prm.a = a;
   prm.advance = advance;
+  prm.merge = s.merge;
   prm.scaler = s.scaler;
   fill_seg(prm.seg, P);
   auto kern = reduce_tree_kernel<MAXSEG, COMP, LEVELS>;
@@ -496,6 +499,7 @@ cudaError_t launch_rs_tree_t(const Plan& P, const float* const* acc, float* cons
   prm.state = st;
   prm.inv = s.inv;
   prm.n = P.n;
+  prm.merge = s.merge;
   fill_seg(prm.seg, P);
   auto kern = rs_tree_kernel<MAXSEG, COMP>;
   kern<<<occupancy_grid(kern, 256, 0, P.ntiles), 256, 0, stream>>>(prm);
@@ -504,27 +508,32 @@ cudaError_t launch_rs_tree_t(const Plan& P, const float* const* acc, float* cons
 
 }  // namespace
 
-cudaError_t launch_reduce_tree(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
-                               const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream,
+cudaError_t launch_reduce_tree(const Plan& P0, const uint16_t* const* g, int a, float* const* gbar,
+                               const StepScalars& s0, int advance0, dp_step_state_t* st, cudaStream_t stream,
                                uint64_t* launches) {
-  ++*launches;
-  const bool comp = s.mode == DP_SUM_COMPENSATED;
-  if (P.nseg <= SMALL_SEG)
-    return comp ? launch_tree_n<SMALL_SEG, true>(P, g, a, gbar, s, advance, st, stream)
-                : launch_tree_n<SMALL_SEG, false>(P, g, a, gbar, s, advance, st, stream);
-  return comp ? launch_tree_n<BIG_SEG, true>(P, g, a, gbar, s, advance, st, stream)
-              : launch_tree_n<BIG_SEG, false>(P, g, a, gbar, s, advance, st, stream);
+  return for_each_chunk(P0, s0, [&](const Plan& P, const StepScalars& s, bool last) {
+    ++*launches;
+    const int advance = (advance0 && last) ? 1 : 0;
+    const bool comp = s.mode == DP_SUM_COMPENSATED;
+    if (P.nseg <= SMALL_SEG)
+      return comp ? launch_tree_n<SMALL_SEG, true>(P, g, a, gbar, s, advance, st, stream)
+                  : launch_tree_n<SMALL_SEG, false>(P, g, a, gbar, s, advance, st, stream);
+    return comp ? launch_tree_n<BIG_SEG, true>(P, g, a, gbar, s, advance, st, stream)
+                : launch_tree_n<BIG_SEG, false>(P, g, a, gbar, s, advance, st, stream);
+  });
 }
 
-cudaError_t launch_rs_tree(const Plan& P, const float* const* acc, float* const* gbar, const StepScalars& s,
+cudaError_t launch_rs_tree(const Plan& P0, const float* const* acc, float* const* gbar, const StepScalars& s0,
                            dp_step_state_t* st, cudaStream_t stream, uint64_t* launches) {
-  ++*launches;
-  const bool comp = s.mode == DP_SUM_COMPENSATED;
-  if (P.nseg <= SMALL_SEG)
-    return comp ? launch_rs_tree_t<SMALL_SEG, true>(P, acc, gbar, s, st, stream)
-                : launch_rs_tree_t<SMALL_SEG, false>(P, acc, gbar, s, st, stream);
-  return comp ? launch_rs_tree_t<BIG_SEG, true>(P, acc, gbar, s, st, stream)
-              : launch_rs_tree_t<BIG_SEG, false>(P, acc, gbar, s, st, stream);
+  return for_each_chunk(P0, s0, [&](const Plan& P, const StepScalars& s, bool) {
+    ++*launches;
+    const bool comp = s.mode == DP_SUM_COMPENSATED;
+    if (P.nseg <= SMALL_SEG)
+      return comp ? launch_rs_tree_t<SMALL_SEG, true>(P, acc, gbar, s, st, stream)
+                  : launch_rs_tree_t<SMALL_SEG, false>(P, acc, gbar, s, st, stream);
+    return comp ? launch_rs_tree_t<BIG_SEG, true>(P, acc, gbar, s, st, stream)
+                : launch_rs_tree_t<BIG_SEG, false>(P, acc, gbar, s, st, stream);
+  });
 }
 
 }  // namespace dp
