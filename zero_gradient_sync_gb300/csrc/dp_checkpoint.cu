@@ -615,14 +615,20 @@ dp_status_t load(const char* root, const char* tag, const dp_layout_t* layout, f
     int32_t k;      // 0 master, 1 m, 2 v
     int32_t ns, os;
   };
+  // Both segment lists are sorted by global offset and tile [0, psi) without gaps, so one sweep over the two
+  // finds every overlap (linear in the segment counts).
   std::vector<Piece> pieces;
-  for (size_t a = 0; a < nsegs.size() && err.code == DP_OK; ++a)
-    for (size_t b = 0; b < osegs.size(); ++b) {
+  size_t b0 = 0;
+  for (size_t a = 0; a < nsegs.size() && err.code == DP_OK; ++a) {
+    const int64_t nend = nsegs[a].goff + nsegs[a].len;
+    while (b0 < osegs.size() && osegs[b0].goff + osegs[b0].len <= nsegs[a].goff) ++b0;
+    for (size_t b = b0; b < osegs.size() && osegs[b].goff < nend; ++b) {
       const int64_t lo = std::max(nsegs[a].goff, osegs[b].goff);
-      const int64_t hi = std::min(nsegs[a].goff + nsegs[a].len, osegs[b].goff + osegs[b].len);
+      const int64_t hi = std::min(nend, osegs[b].goff + osegs[b].len);
       for (int k = 0; k < 3; ++k)
         for (int64_t i = lo; i < hi; i += cap) pieces.push_back({i, std::min(hi - i, cap), k, (int32_t)a, (int32_t)b});
     }
+  }
   float* const* arrays[3] = {master, m, v};
   if (err.code == DP_OK) {
     const int workers = io_workers();
