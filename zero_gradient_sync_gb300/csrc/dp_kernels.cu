@@ -56,6 +56,7 @@ __host__ __device__ constexpr int ra_smem() { return ra_bar_offset<FUSED>() + 2 
 static_assert(ra_smem<0>() + 64 <= 227 * 1024 && ra_smem<1>() + 64 <= 227 * 1024 && ra_smem<2>() + 64 <= 227 * 1024,
               "shared memory fits one CTA");
 static_assert(TILE == RA_CTHREADS * RA_EPT, "one 16-element group per consumer thread");
+static_assert(RA_STATE_FLOATS >= TILE + 8, "a tile's state interior plus its head and tail groups fit one array");
 static_assert(RA_IN_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
 
 template <int MAXSEG>
@@ -74,9 +75,17 @@ struct ReduceParams {
   float* st_m[2][DP_MAX_N];
   float* st_v[2][DP_MAX_N];
   uint16_t* rep[DP_MAX_N];
+  int64_t state_end4[DP_MAX_N];   // each rank's shard length rounded down to a multiple of 4
   float lr, b1f, b2f, eps, omb1, omb2;
   SegTable<MAXSEG> seg;
 };
+
+// Single pass: a tile's old state in shared memory.  Each of the three arrays (RA_STATE_FLOATS apart) holds
+// the tile's 4-aligned local interior [jlo, jhi) from float 4 on, and -- when the tile's local range starts or
+// ends inside a 4-group that lies wholly in the shard array -- that 16-byte head group in floats 0..3 and that
+// tail group right after the interior, so that local element j of the tile is always at 4 + (j - jlo).  Flags
+// say which ragged groups were copied (the shard's last, partial group is read from HBM).
+constexpr int RA_STATE_PAD = 4;
 
 // Ring-buffer position of a stage: slot and the parity of its current use.
 template <int NSTAGES>
@@ -110,7 +119,8 @@ __device__ __forceinline__ void stage_bf16x4(uint16_t* sb, int64_t off, uint32_t
 // old state from set `cur`, new state into the other set, bf16 of the new master into the staging tile.
 template <int MAXSEG>
 __device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, const Tile& t, const AdamK& K, int cur,
-                                             const float* s_g, uint16_t* s_stage, const float* s_state, int tid) {
+                                             const float* s_g, uint16_t* s_stage, const float* s_state,
+                                             const volatile int* s_ragged, int tid) {
   constexpr int UG = 2;
   const int64_t delta = t.loff - t.goff;
   const int64_t cb = (t.start / TILE) * TILE;
@@ -132,9 +142,9 @@ __device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, cons
       if (gq < ngr) {
         const int64_t jj = jlo + 4 * (int64_t)gq;
         // The 4-aligned interior [jlo, jhi) of the old state sits in shared memory (bulk-copied by the producer).
-        t4[u] = *reinterpret_cast<const float4*>(s_state + 4 * gq);
-        m4[u] = *reinterpret_cast<const float4*>(s_state + RA_STATE_FLOATS + 4 * gq);
-        v4[u] = *reinterpret_cast<const float4*>(s_state + 2 * RA_STATE_FLOATS + 4 * gq);
+        t4[u] = *reinterpret_cast<const float4*>(s_state + RA_STATE_PAD + 4 * gq);
+        m4[u] = *reinterpret_cast<const float4*>(s_state + RA_STATE_FLOATS + RA_STATE_PAD + 4 * gq);
+        v4[u] = *reinterpret_cast<const float4*>(s_state + 2 * RA_STATE_FLOATS + RA_STATE_PAD + 4 * gq);
         const float* gs = s_g + (jj - delta - cb);
         g4[u] = galign ? *reinterpret_cast<const float4*>(gs) : make_float4(gs[0], gs[1], gs[2], gs[3]);
       }
@@ -165,7 +175,18 @@ __device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, cons
     if (jx >= je) jx = -1;
   }
   if (jx >= 0) {
-    float th = M[jx], mm = Mm[jx], vv = Vv[jx];
+    // from the copied head / tail group, or (the shard's partial last group) from HBM
+    float th, mm, vv;
+    if (s_ragged[jx < jlo ? 0 : 1]) {
+      const int64_t o = RA_STATE_PAD + (jx - jlo);
+      th = s_state[o];
+      mm = s_state[RA_STATE_FLOATS + o];
+      vv = s_state[2 * RA_STATE_FLOATS + o];
+    } else {
+      th = M[jx];
+      mm = Mm[jx];
+      vv = Vv[jx];
+    }
     adam1(s_g[jx - delta - cb], th, mm, vv, K);
     M2[jx] = th;
     Mm2[jx] = mm;
@@ -181,15 +202,17 @@ __device__ __forceinline__ void fused_update(const ReduceParams<MAXSEG>& p, cons
 struct SpTile {
   int64_t delta, cb, jlo, jhi;
   int cur, owner;
+  const volatile int* ragged;   // the head / tail groups copied into shared memory
 };
 template <int MAXSEG>
 __device__ __forceinline__ void sp_update1(const ReduceParams<MAXSEG>& p, const SpTile& T, const AdamK& K, float g,
                                            int64_t j, const float* s_state, uint16_t* s_stage) {
   float th, mm, vv;
-  if (j >= T.jlo && j < T.jhi) {
-    th = s_state[j - T.jlo];
-    mm = s_state[RA_STATE_FLOATS + (j - T.jlo)];
-    vv = s_state[2 * RA_STATE_FLOATS + (j - T.jlo)];
+  if ((j >= T.jlo && j < T.jhi) || T.ragged[j < T.jlo ? 0 : 1]) {
+    const int64_t o = RA_STATE_PAD + (j - T.jlo);
+    th = s_state[o];
+    mm = s_state[RA_STATE_FLOATS + o];
+    vv = s_state[2 * RA_STATE_FLOATS + o];
   } else {
     th = p.st_master[T.cur][T.owner][j];
     mm = p.st_m[T.cur][T.owner][j];
@@ -206,9 +229,9 @@ template <int MAXSEG>
 __device__ __forceinline__ void sp_update4(const ReduceParams<MAXSEG>& p, const SpTile& T, const AdamK& K, float g0,
                                            float g1, float g2, float g3, int64_t j, const float* s_state,
                                            uint16_t* s_stage) {
-  float4 th = *reinterpret_cast<const float4*>(s_state + (j - T.jlo));
-  float4 mm = *reinterpret_cast<const float4*>(s_state + RA_STATE_FLOATS + (j - T.jlo));
-  float4 vv = *reinterpret_cast<const float4*>(s_state + 2 * RA_STATE_FLOATS + (j - T.jlo));
+  float4 th = *reinterpret_cast<const float4*>(s_state + RA_STATE_PAD + (j - T.jlo));
+  float4 mm = *reinterpret_cast<const float4*>(s_state + RA_STATE_FLOATS + RA_STATE_PAD + (j - T.jlo));
+  float4 vv = *reinterpret_cast<const float4*>(s_state + 2 * RA_STATE_FLOATS + RA_STATE_PAD + (j - T.jlo));
   adam1(g0, th.x, mm.x, vv.x, K);
   adam1(g1, th.y, mm.y, vv.y, K);
   adam1(g2, th.z, mm.z, vv.z, K);
@@ -264,6 +287,8 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
   __shared__ float s_inv;
   __shared__ float s_k[2];
   __shared__ int s_cur;
+  __shared__ int s_ragged_buf[2];   // single pass: the current tile's head / tail state groups are in s_state
+  volatile int* s_ragged = s_ragged_buf;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = p.n, a = p.a;
@@ -329,13 +354,24 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
             return;
           }
           const int64_t delta = t.loff - t.goff;
-          const int64_t jlo = (t.start + delta + 3) & ~int64_t(3), jhi = (t.end + delta) & ~int64_t(3);
+          const int64_t js = t.start + delta, je = t.end + delta;
+          const int64_t jlo = (js + 3) & ~int64_t(3), jhi = je & ~int64_t(3);
+          const int64_t end4 = p.state_end4[t.owner];
           const uint32_t sb = jhi > jlo ? (uint32_t)(jhi - jlo) * 4u : 0u;
-          mbar_arrive_expect_tx(smem_u32(sfull), 3u * sb);
-          if (sb) {
-            bulk_g2s(smem_u32(s_state), p.st_master[s_cur][t.owner] + jlo, sb, smem_u32(sfull));
-            bulk_g2s(smem_u32(s_state + RA_STATE_FLOATS), p.st_m[s_cur][t.owner] + jlo, sb, smem_u32(sfull));
-            bulk_g2s(smem_u32(s_state + 2 * RA_STATE_FLOATS), p.st_v[s_cur][t.owner] + jlo, sb, smem_u32(sfull));
+          // The head group [jlo - 4, jlo) when the range starts inside it, the tail group [jhi, jhi + 4) when it
+          // ends inside it (the same group as the head when no whole group lies inside the range), each only
+          // when it lies wholly in the array.
+          const bool head = (js & 3) != 0 && jlo <= end4;
+          const bool tail = (je & 3) != 0 && jhi >= jlo && jhi + 4 <= end4;
+          s_ragged[0] = head ? 1 : 0;
+          s_ragged[1] = (tail || (jhi < jlo && head)) ? 1 : 0;
+          mbar_arrive_expect_tx(smem_u32(sfull), 3u * (sb + (head ? 16u : 0u) + (tail ? 16u : 0u)));
+          float* const src[3] = {p.st_master[s_cur][t.owner], p.st_m[s_cur][t.owner], p.st_v[s_cur][t.owner]};
+          for (int k = 0; k < 3; ++k) {
+            float* dst = s_state + k * RA_STATE_FLOATS;
+            if (sb) bulk_g2s(smem_u32(dst + RA_STATE_PAD), src[k] + jlo, sb, smem_u32(sfull));
+            if (head) bulk_g2s(smem_u32(dst + RA_STATE_PAD - 4), src[k] + (jlo - 4), 16u, smem_u32(sfull));
+            if (tail) bulk_g2s(smem_u32(dst + RA_STATE_PAD + (jhi - jlo)), src[k] + jhi, 16u, smem_u32(sfull));
           }
           ++sit;
         };
@@ -527,7 +563,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
           live = false;
         }
         if constexpr (FUSED == 1) {
-          fused_update(p, t, K, s_cur, s_g, s_stage, s_state, tid);
+          fused_update(p, t, K, s_cur, s_g, s_stage, s_state, s_ragged, tid);
         } else {
           // Every thread updates the elements whose gbar it holds: with every shard offset a multiple of 4 (the
           // launcher's condition for this variant) a thread's 16 elements are four aligned 4-groups in local
@@ -539,6 +575,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) reduce_kernel(const __grid_cons
           T.jhi = (t.end + T.delta) & ~int64_t(3);
           T.cur = s_cur;
           T.owner = t.owner;
+          T.ragged = s_ragged;
           const int64_t Lt = e0 + T.delta;
           if (whole && (Lt & 3) == 0) {
 #pragma unroll
@@ -1074,6 +1111,7 @@ static cudaError_t launch_reduce_t(const Plan& P, const uint16_t* const* g, int 
         prm.st_v[k][r] = fa->v[k * P.n + r];
       }
       prm.rep[r] = fa->rep[r];
+      prm.state_end4[r] = P.shard_len[r] & ~int64_t(3);
     }
   }
   prm.lr = s.lr;
