@@ -125,3 +125,33 @@ def test_micro_argument_checks(dev):
     rc = dp.LIB.dp_reduce_scatter_micro(None, None, None, dp._lib._ptr_array(g), 0, 2, dp._lib.ctypes.byref(c.layout.c),
                                         A, 1.0, COMP, b.state.data_ptr(), 0)
     assert rc == dp.DP_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("inject", [False, True])
+def test_micro_deferred_commit_equals_direct(dev, inject):
+    """The per-micro-step form with DP_DEFER_COMMIT on its calls (the step split across GPUs) and
+    DP_DEVICE_SCALE: the last call publishes the decision without committing; dp_commit_step with the scaler then
+    commits (or, with a NaN in one micro-step, skips and backs the scale off) and dp_step_update finishes.  The
+    result equals, byte for byte, dp_step_scaled's -- the same order of ranks within each micro-step only when
+    a = 1, so the comparison runs at a = 1 -- and the state words (t, scale, clean-step count) agree."""
+    wl = BASE.with_(psi=250_003, n=4, a=1, stage=2, layout="ragged", seed=41, loss_scale=2.0 ** 12)
+    c = gu.make_case(wl)
+    A = adam_of(wl)
+    sc = dp.scaler(2.0, 0.5, 2, 2.0 ** 8, 2.0 ** 24)
+    ref = gu.upload(c)
+    b = upload_micro(c)
+    for x in (ref, b):
+        dp.dp_scaler_init(x.state, wl.loss_scale)
+        if inject:
+            x.grad(2, 0)[777:778].view(torch.int16).fill_(synth.BF16_NAN)
+    for _ in range(3):
+        ref.step_scaled(A, sc)
+        b.reduce_micro(0, A, 1.0, COMP | dp.DP_DEFER_COMMIT | dp.DP_DEVICE_SCALE)
+        mid = dp.read_state(b.state)
+        assert mid["found_inf"] == int(inject)
+        dp.dp_commit_step(b.state, A, sc)
+        b.update(A)
+        r, g = dp.read_state(ref.state), dp.read_state(b.state)
+        for key in ("t", "found_inf", "nonfinite", "loss_scale", "good_steps", "b1t", "b2t", "error"):
+            assert g[key] == r[key], key
+        assert gu.snapshot(b) == gu.snapshot(ref)
