@@ -112,3 +112,27 @@ def test_scaler_argument_checks(dev):
         b.step_scaled(dp.adam(), dp.scaler(growth_factor=0.5))
     with pytest.raises(dp.DPError):
         b.step_scaled(dp.adam(), dp.scaler(min_scale=4.0, max_scale=2.0))
+
+
+def test_single_pass_with_device_scale_equals_fixed_scale(dev):
+    """dp_step_single_pass with DP_DEVICE_SCALE unscales by the device-resident scale: with that scale set to S it
+    equals the single pass at the fixed loss scale S byte for byte, and without a deferred commit it leaves the
+    scale as it was (the policy runs only in dp_step_scaled or a commit given a scaler)."""
+    S = 2.0 ** 14
+    wl = BASE.with_(loss_scale=S)
+    c = gu.make_case(wl)
+    A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
+    fixed = gu.upload(c, second_set=True)
+    dev_scale = gu.upload(c, second_set=True)
+    dp.dp_scaler_init(dev_scale.state, S)
+    for _ in range(2):
+        fixed.step_single_pass(A, S)
+        dev_scale.step_single_pass(A, 1.0, dp.DP_SUM_COMPENSATED | dp.DP_DEVICE_SCALE)
+    a, b = dp.read_state(fixed.state), dp.read_state(dev_scale.state)
+    assert (b["t"], b["cur_set"], b["loss_scale"], b["good_steps"]) == (a["t"], a["cur_set"], S, 0)
+
+    def current(x):
+        torch.cuda.synchronize()
+        ms, mm, vv = x.current()
+        return [t.detach().cpu().view(torch.uint8).numpy().tobytes() for t in ms + mm + vv + x.replicas]
+    assert current(fixed) == current(dev_scale)
