@@ -270,3 +270,21 @@ def test_step_flags_accepted_only_where_documented(dp):
         dp.dp_commit_single_pass(fake[:2], fake[:4], dp.Layout(0, 2, 16, [(0, 8, 0, 0), (8, 8, 1, 0)]), A, 256,
                                  stream=0)
     assert dp.dp_kernel_launches() == before
+
+
+def test_layouts_beyond_one_launch_table_validate(dp):
+    """Layouts of more than DP_KERNEL_SEG segments are accepted on the host (each kernel then runs as several
+    launches); shard lengths and the workspace follow the segments; more than DP_MAX_SEG is refused."""
+    import synth
+    psi, n = 1_000_003, 8
+    segs = synth.layout_random(psi, n, 5000, seed=9)
+    L = dp.Layout(2, n, psi, segs)
+    L.validate()
+    assert len([s for s in segs if s[1]]) > dp.DP_KERNEL_SEG
+    assert L.shard_lens() == synth.shard_lengths(segs, n)
+    assert L.workspace_size() == sum((4 * x + 255) // 256 * 256 for x in L.shard_lens())
+    B = dp.Layout.even(psi, 4, stage=3, bucket=700, misalign=3)      # 1429 buckets x 4 = 5716 segments
+    assert len(B.segs) == 4 * ((psi + 699) // 700)
+    B.validate()
+    with pytest.raises(dp.DPError):
+        dp.Layout.even(dp.DP_MAX_SEG + 1, 2, bucket=1)
