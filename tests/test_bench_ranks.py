@@ -1,5 +1,6 @@
-"""The benchmark's multi-rank path on CPU (gloo, world size 2): replicas only -- a barrier, the max of the
-ranks' times, and whole-job throughput; no collective touches the data path."""
+"""The benchmark's multi-rank timing on CPU (gloo, world size 2): a barrier, the max of the ranks' times, and
+whole-job throughput (each rank's slice is one workload, so the job processes world_size workloads a step).
+The slices' shared skip decision is tested in test_sliced_ranks.py."""
 import os
 import socket
 import sys

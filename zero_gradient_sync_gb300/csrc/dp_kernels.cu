@@ -12,10 +12,18 @@
 //   (16-byte vector loads/stores in local index space) and the bf16 image of
 //   the new master staged in shared memory, then bulk-stored into all n
 //   replicas (cp.async.bulk shared->global) at global index.
+// single pass (reduce with FUSED != 0): pass A's stream, then each tile's
+//   update from gbar on chip and the tile's old optimizer state, bulk-copied
+//   into shared memory while its gradients stream, into the other of two
+//   state sets (made current by the last CTA unless skipped); repair rewrites
+//   the replicas on a skipped step.
+// update, plain data parallelism (stage 0): every rank's full-length state
+//   updated with the owner's gbar, 16-byte vectors over (rank, 4-group) items.
 // Staged kernels (accumulate, rs_avg, adam = update without replicas,
 //   allgather, advance) compute the same step one phase at a time: bit-
 //   identical in plain arithmetic; compensated, the staged form keeps one
 //   (hi, lo) pair per rank where pass A carries one pair through all inputs.
+// commit: the step state's commit for a reduction that deferred it.
 #include <algorithm>
 #include <type_traits>
 
