@@ -140,11 +140,21 @@ def micro_bytes(wl, comp: bool) -> int:
     return 2 * wl.n * wl.a + acc + 2 * acc * (wl.a - 2) + acc + 4
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and blank space, so that a comment edit does not mark a kernel as
+    changed."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel="reduce"):
+    """sha256 prefix of the code (comments and spacing removed) of the files that make up a kernel."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "zero_gradient_sync_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "zero_gradient_sync_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
