@@ -288,3 +288,24 @@ def test_layouts_beyond_one_launch_table_validate(dp):
     B.validate()
     with pytest.raises(dp.DPError):
         dp.Layout.even(dp.DP_MAX_SEG + 1, 2, bucket=1)
+
+
+def test_single_pass_from_host_argument_errors_queue_nothing(dp):
+    """dp_step_single_pass_from_host checks every argument before it queues a copy or a kernel (no GPU needed)."""
+    import ctypes
+    L = dp.Layout(1, 2, 16, [(0, 8, 0, 0), (8, 8, 1, 0)])
+    two, four = ctypes.c_void_p * 2, ctypes.c_void_p * 4
+    fake, null = two(16, 32), two(0, 0)
+    st4 = four(16, 32, 48, 64)
+    A = dp.adam()
+    f = dp.LIB.dp_step_single_pass_from_host
+    before = dp.dp_kernel_launches()
+    assert f(fake, st4, st4, st4, fake, fake, 0, ctypes.byref(L.c), A, 1.0, 0, 256, None, None) == dp.DP_ERR_INVALID_ARG
+    assert f(fake, st4, st4, st4, None, fake, 1, ctypes.byref(L.c), A, 1.0, 0, 256, None, None) == dp.DP_ERR_INVALID_ARG
+    assert f(fake, st4, st4, st4, null, fake, 1, ctypes.byref(L.c), A, 1.0, 0, 256, None, None) != dp.DP_OK
+    assert f(fake, st4, st4, st4, fake, two(16, 17), 1, ctypes.byref(L.c), A, 1.0, 0, 256, None,
+             None) == dp.DP_ERR_ALIGNMENT
+    assert f(fake, st4, st4, st4, fake, fake, 1, ctypes.byref(L.c), A, 1.0, 0, None, None, None) == dp.DP_ERR_INVALID_ARG
+    assert f(fake, st4, st4, st4, fake, fake, 1, ctypes.byref(L.c), A, 1.0, dp.DP_ORDER_TREE, 256, None,
+             None) == dp.DP_ERR_INVALID_ARG
+    assert dp.dp_kernel_launches() == before
