@@ -29,7 +29,9 @@
  *    traffic; "DP gradient sync at scale": 2(N-1) ring steps.
  *  The pages name Adam but do not print its equations; the library uses
  *  standard Adam (Kingma & Ba 2015) with bias correction, epsilon added to
- *  sqrt(vhat), no weight decay.  Loss-scale unscaling and the skipped step
+ *  sqrt(vhat), no weight decay, in fp32 (the moments correctly rounded, the
+ *  update's square root and division by the GPU's approximate instructions,
+ *  within a few ulp of the update term).  Loss-scale unscaling and the skipped step
  *  are not spelled out on the pages either: gbar is multiplied by
  *  fl32(1 / (n S)) and any non-finite value skips the whole step.
  *
