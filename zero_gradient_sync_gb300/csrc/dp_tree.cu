@@ -366,6 +366,297 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
                      p.merge);
 }
 
+// ---------------------------------------------------------------- compensated, n <= 8: rank-major stages
+//
+// reduce_tree_rm_kernel: the compensated tree for a compile-time rank count N <= 8.  A stage holds micro-step k
+// of every rank for one sub-tile (N bulk copies on one barrier).  Each consumer thread carries the N ranks'
+// (hi, lo) leaf sums of its EPT elements across the micro-steps -- N * EPT / 2 independent packed lanes, where
+// the binary counter above has EPT / 2 -- and after the last micro-step adds the leaves up the binomial tree
+// level by level, every merge fixed at compile time: no pending slots and no rank-dependent branches.  Each
+// leaf is the same chain and each merge the same operation on the same operands as in the binary counter, so
+// the result is the same bits.  EPT * N = 32 for N >= 2: a stage is 30 KB or less, and the leaves take 64
+// registers a thread at most.
+constexpr int RM_MAX_STAGES = 12;
+template <int N>
+__host__ __device__ constexpr int rm_ept() { return N <= 2 ? 16 : (N <= 4 ? 8 : 4); }
+template <int N>
+__host__ __device__ constexpr int rm_sub() { return TT_CTHREADS * rm_ept<N>(); }      // elements of a sub-tile
+template <int N>
+__host__ __device__ constexpr int rm_in_bytes() { return 2 * rm_sub<N>(); }         // one input's sub-tile
+template <int N>
+__host__ __device__ constexpr int rm_stages() {
+  return TT_RING_BYTES / (N * rm_in_bytes<N>()) < RM_MAX_STAGES ? TT_RING_BYTES / (N * rm_in_bytes<N>())
+                                                                : RM_MAX_STAGES;
+}
+static_assert(RM_MAX_STAGES <= TT_MAX_STAGES, "the barriers fit the tree kernel's shared layout");
+static_assert(TILE % rm_sub<8>() == 0 && TILE % rm_sub<4>() == 0 && TILE % rm_sub<2>() == 0,
+              "a tile is a whole number of sub-tiles");
+static_assert(rm_sub<8>() % 8 == 0 && rm_in_bytes<8>() % 16 == 0, "sub-tiles start on 16-byte boundaries");
+static_assert(rm_stages<8>() >= 4 && rm_stages<7>() >= 4, "at least four stages in flight");
+
+// The range of sub-tile h (SUB elements) of a tile, copied as the 8-aligned hull (as half_of).
+__device__ __forceinline__ Half sub_of(const Tile& t, int h, int sub) {
+  const int64_t cb = (t.start / TILE) * TILE + (int64_t)h * sub;
+  Half x;
+  x.lo = t.start > cb ? t.start : cb;
+  x.hi = t.end < cb + sub ? t.end : cb + sub;
+  x.sa = x.lo & ~int64_t(7);
+  return x;
+}
+
+// EPT bf16 (EPT / 2 words) from shared memory: one 8- or 16-byte load, or two 16-byte loads.
+template <int EPT>
+__device__ __forceinline__ void rm_load(const unsigned char* s, uint32_t (&w)[EPT / 2]) {
+  if constexpr (EPT == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(s);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int c = 0; c < EPT / 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(s + 16 * c);
+      w[4 * c + 0] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+    }
+  }
+}
+
+// One micro-step of every rank into the leaves: the first sets (h, l) = (x, 0), later ones
+// (h, e) = TwoSum(h, x), l = l + e.
+template <int N, int W, bool FIRST>
+__device__ __forceinline__ void rm_fold(f2_t (&h)[N][W], f2_t (&l)[N][W], const uint32_t (&w)[N][W]) {
+#pragma unroll
+  for (int r = 0; r < N; ++r)
+#pragma unroll
+    for (int u = 0; u < W; ++u) {
+      const f2_t x = bf16x2_to_f2(w[r][u]);
+      if (FIRST) {
+        h[r][u] = x;
+        l[r][u] = 0ull;
+      } else {
+        f2_t e;
+        h[r][u] = f2_two_sum(h[r][u], x, e);
+        l[r][u] = f2_add(l[r][u], e);
+      }
+    }
+}
+
+// One level of the binomial tree over the leaves: block r (a multiple of 2 STEP) takes block r + STEP on its
+// right, (H, e) = TwoSum(H_r, H_right), L = (L_r + e) + L_right; a block with no partner stays.
+template <int N, int W, int STEP>
+__device__ __forceinline__ void rm_level(f2_t (&h)[N][W], f2_t (&l)[N][W]) {
+#pragma unroll
+  for (int r = 0; r + STEP < N; r += 2 * STEP)
+#pragma unroll
+    for (int u = 0; u < W; ++u) {
+      f2_t e;
+      const f2_t H = f2_two_sum(h[r][u], h[r + STEP][u], e);
+      l[r][u] = f2_add(f2_add(l[r][u], e), l[r + STEP][u]);
+      h[r][u] = H;
+    }
+}
+// The whole tree, levels 0, 1, 2 in turn; the total is left in leaf 0.
+template <int N, int W>
+__device__ __forceinline__ void rm_tree(f2_t (&h)[N][W], f2_t (&l)[N][W]) {
+  if constexpr (N > 1) rm_level<N, W, 1>(h, l);
+  if constexpr (N > 2) rm_level<N, W, 2>(h, l);
+  if constexpr (N > 4) rm_level<N, W, 4>(h, l);
+}
+
+template <int MAXSEG, int N>
+__global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __grid_constant__ TreeParams<MAXSEG> p) {
+  constexpr int EPT = rm_ept<N>();
+  constexpr int W = EPT / 2;
+  constexpr int SUB = rm_sub<N>();
+  constexpr int IN = rm_in_bytes<N>();
+  constexpr int SBY = N * IN;
+  constexpr int NST = rm_stages<N>();
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TT_RING_BYTES);
+  uint64_t* empty = full + NST;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + NST);
+  unsigned long long* s_count = reinterpret_cast<unsigned long long*>(empty + NST + 1);
+  __shared__ float s_inv;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int a = p.a;
+  const int ntiles = p.seg.ntiles;
+  const int64_t psi = p.seg.psi;
+  const int64_t p8 = psi & ~int64_t(7);
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), TT_CWARPS);
+    }
+    *s_abort = 0;
+    *s_count = 0ull;
+    float inv = p.inv;
+    if (p.scaler.enabled) {
+      // fl32(1 / (n S)) from the device-resident scale, as for the ring order.
+      const float sc = *reinterpret_cast<volatile const float*>(&p.state->loss_scale);
+      inv = (float)(1.0 / ((double)p.n * (double)sc));
+      if (!(sc > 0.0f) || nonfinite(sc) || !(inv >= 1.17549435e-38f) || nonfinite(inv)) {
+        record_error(p.state, DP_ERR_INVALID_ARG);
+        *s_abort = 1;
+        inv = 0.0f;
+      }
+    }
+    s_inv = inv;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  unsigned bad = 0;
+  if (warp == TT_CWARPS) {
+    // ------------------------------------------------------------ producer: per sub-tile, micro-step k of every rank
+    if (lane == 0) {
+      StagePos<NST> sp;
+      TileWalker<MAXSEG> walk;
+      for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
+        const Tile t = walk.at(p.seg, tile);
+        for (int h = 0; h < TILE / SUB && !*s_abort; ++h) {
+          const Half x = sub_of(t, h, SUB);
+          if (x.empty()) continue;
+          int64_t sb = (x.hi + 7) & ~int64_t(7);
+          if (sb > p8) sb = p8;
+          const uint32_t bytes = sb > x.sa ? (uint32_t)(sb - x.sa) * 2u : 0u;
+          for (int k = 0; k < a && !*s_abort; ++k) {
+            if (sp.count >= (uint32_t)NST &&
+                !mbar_wait_bounded(smem_u32(&empty[sp.slot]), sp.phase ^ 1u, p.timeout_ns, s_abort)) {
+              if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+              *s_abort = 1;
+              break;
+            }
+            const uint32_t fb = smem_u32(&full[sp.slot]);
+            mbar_arrive_expect_tx(fb, bytes * (uint32_t)N);
+            if (bytes)
+              for (int r = 0; r < N; ++r)
+                bulk_g2s(smem_u32(stages + sp.slot * SBY + r * IN), p.g[r * a + k] + x.sa, bytes, fb);
+            sp.next();
+          }
+        }
+      }
+      // Never leave with copies in flight: wait for the newest issued phase of every slot.
+      if (*s_abort) {
+        const uint32_t it = sp.count;
+        const uint32_t first = it > (uint32_t)NST ? it - NST : 0u;
+        for (uint32_t y = first; y < it; ++y)
+          (void)mbar_wait_bounded(smem_u32(&full[y % NST]), (y / NST) & 1u, p.timeout_ns, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumers: EPT elements of N ranks per thread
+    const f2_t inv2 = f2_pack(s_inv, s_inv);
+    StagePos<NST> sp;
+    TileWalker<MAXSEG> walk;
+    bool live = true;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const Tile t = walk.at(p.seg, tile);
+      for (int h = 0; h < TILE / SUB; ++h) {
+        const Half x = sub_of(t, h, SUB);
+        if (x.empty()) continue;
+        const int64_t e0 = x.sa + EPT * tid;
+        const bool active = e0 < x.hi;
+        const bool tailgrp = active && (e0 + EPT > p8);
+
+        // One stage (micro-step k): wait for its bytes, take this thread's EPT values of every rank, release the
+        // slot.  WHOLE (a whole sub-tile below the buffer's last partial 8-group): shared loads only.
+        // Otherwise inactive threads take zeros and the tail group is read from global memory.
+        auto take = [&](auto whole_tag, int k, uint32_t (&w)[N][W]) {
+          constexpr bool WHOLE = decltype(whole_tag)::value;
+          if (live && !mbar_wait_bounded(smem_u32(&full[sp.slot]), sp.phase, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+            *s_abort = 1;
+            live = false;
+          }
+          const unsigned char* src_s = stages + sp.slot * SBY + 2 * EPT * tid;
+          if constexpr (WHOLE) {
+#pragma unroll
+            for (int r = 0; r < N; ++r) rm_load<EPT>(src_s + r * IN, w[r]);
+          } else {
+#pragma unroll
+            for (int r = 0; r < N; ++r)
+#pragma unroll
+              for (int u = 0; u < W; ++u) w[r][u] = 0u;
+            if (active && live) {
+#pragma unroll
+              for (int r = 0; r < N; ++r) {
+                if (!tailgrp) {
+                  rm_load<EPT>(src_s + r * IN, w[r]);
+                } else {
+                  const uint16_t* src = p.g[r * a + k];
+#pragma unroll
+                  for (int u = 0; u < EPT; ++u) {
+                    const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
+                    w[r][u >> 1] |= (u & 1) ? (b << 16) : b;
+                  }
+                }
+              }
+            }
+          }
+          // The slot is refilled by the async proxy: order this thread's reads of it before that write.
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty[sp.slot]));
+          sp.next();
+        };
+
+        // The leaves over the micro-steps, then the tree.
+        f2_t hs[N][W], ls[N][W];
+        auto run = [&](auto whole_tag) {
+          {
+            uint32_t w[N][W];
+            take(whole_tag, 0, w);
+            rm_fold<N, W, true>(hs, ls, w);
+          }
+          for (int k = 1; k < a; ++k) {
+            uint32_t w[N][W];
+            take(whole_tag, k, w);
+            rm_fold<N, W, false>(hs, ls, w);
+          }
+        };
+        if (x.hi - x.lo == SUB && x.hi <= p8) run(std::true_type{});
+        else run(std::false_type{});
+        rm_tree<N, W>(hs, ls);
+
+        float o[EPT];
+#pragma unroll
+        for (int u = 0; u < W; ++u) f2_unpack(f2_mul(f2_add(hs[0][u], ls[0][u]), inv2), o[2 * u], o[2 * u + 1]);
+        if (active) {
+          float* dst = p.gbar[t.owner] + (t.loff + (e0 - t.goff));
+          const bool all = e0 >= x.lo && e0 + EPT <= x.hi;
+          if (all && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+#pragma unroll
+            for (int c = 0; c < EPT / 4; ++c)
+              *reinterpret_cast<float4*>(dst + 4 * c) = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+#pragma unroll
+            for (int u = 0; u < EPT; ++u) bad += nonfinite(o[u]);
+          } else {
+#pragma unroll
+            for (int u = 0; u < EPT; ++u)
+              if (e0 + u >= x.lo && e0 + u < x.hi) {
+                dst[u] = o[u];
+                bad += nonfinite(o[u]);
+              }
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ CTA total, then the grid's
+  unsigned long long c = bad;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+  __syncthreads();
+  if (lane == 0 && c) atomicAdd(s_count, c);
+  __syncthreads();
+  if (tid == 0)
+    finish_reduction(p.state, *s_count, (*s_count != 0ull) || *s_abort, p.advance, p.beta1, p.beta2, &p.scaler, 0,
+                     p.merge);
+}
+
 // ---------------------------------------------------------------- staged: the tree over per-rank accumulators
 
 template <int MAXSEG>
@@ -448,9 +739,9 @@ __global__ void __launch_bounds__(256) rs_tree_kernel(const __grid_constant__ Rs
 
 // ---------------------------------------------------------------- launchers
 
-template <int MAXSEG, bool COMP, int LEVELS>
-cudaError_t launch_tree_t(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
-                          const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream) {
+template <int MAXSEG>
+TreeParams<MAXSEG> tree_params(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
+                               const StepScalars& s, int advance, dp_step_state_t* st) {
   TreeParams<MAXSEG> prm;
   for (int q = 0; q < P.n * a; ++q) prm.g[q] = g[q];
   for (int r = 0; r < P.n; ++r) prm.gbar[r] = gbar[r];
@@ -465,27 +756,48 @@ cudaError_t launch_tree_t(const Plan& P, const uint16_t* const* g, int a, float*
   prm.merge = s.merge;
   prm.scaler = s.scaler;
   fill_seg(prm.seg, P);
-  auto kern = reduce_tree_kernel<MAXSEG, COMP, LEVELS>;
+  return prm;
+}
+
+template <auto KERN, int MAXSEG>
+cudaError_t launch_tree_kernel(const TreeParams<MAXSEG>& prm, int ntiles, cudaStream_t stream) {
   // The opt-in shared-memory size is set once per device (not inside a stream capture on later calls).
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TT_SMEM);
+    e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, TT_SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   // One CTA per SM (every CTA joins the grid-wide finish, so at least one runs even with no tiles).
-  kern<<<occupancy_grid(kern, TT_THREADS, TT_SMEM, P.ntiles), TT_THREADS, TT_SMEM, stream>>>(prm);
+  KERN<<<occupancy_grid(KERN, TT_THREADS, TT_SMEM, ntiles), TT_THREADS, TT_SMEM, stream>>>(prm);
   return cudaGetLastError();
 }
 
+// Compensated with n <= 8: the rank-major kernel for that n.  Otherwise the binary counter (n <= 8 plain,
+// n <= 16 either arithmetic).
 template <int MAXSEG, bool COMP>
 cudaError_t launch_tree_n(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
                           const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream) {
-  if (P.n <= 8) return launch_tree_t<MAXSEG, COMP, 3>(P, g, a, gbar, s, advance, st, stream);
-  return launch_tree_t<MAXSEG, COMP, 4>(P, g, a, gbar, s, advance, st, stream);
+  const TreeParams<MAXSEG> prm = tree_params<MAXSEG>(P, g, a, gbar, s, advance, st);
+  if constexpr (COMP) {
+    switch (P.n) {
+      case 1: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 1>, MAXSEG>(prm, P.ntiles, stream);
+      case 2: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 2>, MAXSEG>(prm, P.ntiles, stream);
+      case 3: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 3>, MAXSEG>(prm, P.ntiles, stream);
+      case 4: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 4>, MAXSEG>(prm, P.ntiles, stream);
+      case 5: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 5>, MAXSEG>(prm, P.ntiles, stream);
+      case 6: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 6>, MAXSEG>(prm, P.ntiles, stream);
+      case 7: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 7>, MAXSEG>(prm, P.ntiles, stream);
+      case 8: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 8>, MAXSEG>(prm, P.ntiles, stream);
+      default: return launch_tree_kernel<reduce_tree_kernel<MAXSEG, true, 4>, MAXSEG>(prm, P.ntiles, stream);
+    }
+  } else {
+    if (P.n <= 8) return launch_tree_kernel<reduce_tree_kernel<MAXSEG, false, 3>, MAXSEG>(prm, P.ntiles, stream);
+    return launch_tree_kernel<reduce_tree_kernel<MAXSEG, false, 4>, MAXSEG>(prm, P.ntiles, stream);
+  }
 }
 
 template <int MAXSEG, bool COMP>
