@@ -41,6 +41,10 @@ CASES = [
     (40_961, 16, 4, 2, "even", {}),
     (33_335, 13, 2, 0, "random", {"nseg": 9}),
     (20_000, 6, 8, 1, "ragged", {}),
+    (2 * 7680 + 1919, 4, 3, 3, "random", {"nseg": 7}),
+    (3 * 7680 + 961, 9, 1, 1, "ragged", {}),
+    (50_001, 12, 2, 2, "buckets", {"bucket": 4_000, "misalign": 3}),
+    (30_721, 15, 3, 3, "even", {}),
 ]
 
 

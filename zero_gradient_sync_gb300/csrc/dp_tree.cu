@@ -8,12 +8,14 @@
 // of two) goes up a level unchanged.  The order does not depend on the shard owner (the all-reduce root is
 // rank 0 for every element); each owner keeps its shard of the result.
 //
-// reduce_tree_kernel: the ring kernel's stream -- one producer thread issuing 1-D bulk copies of every input
-// into a ring of shared-memory stages, bounded mbarrier waits -- with a consumer that keeps the tree as a
-// binary counter: slot l holds the pending sum of a complete block of 2^l ranks, so at most log2(n) partial
-// sums are live, each in registers.  To leave room for them a consumer thread owns 8 elements (the ring
-// kernel's 16), so a stage input is half a tile (3840 elements, a 7.5 KB copy); plain arithmetic puts four
-// inputs on a stage, compensated one.  Whole half tiles take a loop without per-input guards.
+// Both pass-A kernels take the ring kernel's stream: one producer thread issuing 1-D bulk copies into a ring
+// of shared-memory stages, bounded mbarrier waits.
+// reduce_tree_kernel (plain arithmetic): consumers keep the tree as a binary counter -- slot l holds the
+// pending sum of a complete block of 2^l ranks, so at most log2(n) partial sums are live, each in registers.
+// A consumer thread owns 8 elements (the ring kernel's 16), so a stage input is half a tile (3840 elements, a
+// 7.5 KB copy), four inputs to a stage.  Whole half tiles take a loop without per-input guards.
+// reduce_tree_rm_kernel (compensated arithmetic): a stage holds one micro-step of every rank; each thread
+// carries every rank's (hi, lo) leaf and adds the leaves up a tree fixed at compile time (below).
 // rs_tree_kernel: the same tree over the staged per-rank accumulators, one element per thread.
 #include <type_traits>
 
@@ -31,18 +33,14 @@ constexpr int TT_THREADS = TT_CTHREADS + 32;       // + one producer warp
 constexpr int TT_SUB = TT_CTHREADS * TT_EPT;       // elements of a stage input: half a tile
 constexpr int TT_IN_BYTES = TT_SUB * 2;            // one input's half tile: a 7.5 KB bulk copy
 constexpr int TT_RING_BYTES = 24 * TT_IN_BYTES;    // 180 KB of stages in flight
-constexpr int TT_MAX_STAGES = 24;
+constexpr int TT_MAX_STAGES = 12;                  // barrier pairs reserved (either kernel)
 constexpr int TT_SMEM = TT_RING_BYTES + 2 * TT_MAX_STAGES * 8 + 32;
 constexpr int RT_LEVELS = 5;                       // staged kernel: slots for n <= 16 (levels 0..4)
-// Inputs per stage: four in plain arithmetic; one when the compensated pending sums (hi and lo pairs) take
-// the registers.
-template <int LEVELS, bool COMP>
-__host__ __device__ constexpr int tt_nps() { return COMP ? 1 : 4; }
-template <int LEVELS, bool COMP>
-__host__ __device__ constexpr int tt_stages() { return TT_RING_BYTES / (tt_nps<LEVELS, COMP>() * TT_IN_BYTES); }
+constexpr int TT_NPS = 4;                          // binary counter: inputs per stage
+constexpr int TT_STAGES = TT_RING_BYTES / (TT_NPS * TT_IN_BYTES);
 static_assert(TILE == 2 * TT_SUB, "a tile is two half tiles");
 static_assert(TT_IN_BYTES % 16 == 0, "bulk copies are whole 16-byte units");
-static_assert(tt_stages<4, true>() <= TT_MAX_STAGES && tt_stages<4, false>() <= TT_MAX_STAGES, "barriers fit");
+static_assert(TT_STAGES <= TT_MAX_STAGES, "barriers fit");
 static_assert(TT_SMEM + 64 <= 227 * 1024, "shared memory fits one CTA");
 
 template <int MAXSEG>
@@ -59,26 +57,16 @@ struct TreeParams {
   SegTable<MAXSEG> seg;
 };
 
-// Eight elements' partial sum: packed hi pairs and (compensated) their accumulated rounding errors.
+// Eight elements' partial sum: four packed pairs.
 struct Part8 {
-  f2_t h[4], l[4];
+  f2_t h[4];
 };
 
-// left + right, left being the lower-index block: (H, e) = TwoSum(left.H, right.H), L = (left.L + e) + right.L.
-template <bool COMP>
+// left + right, left being the lower-index block.
 __device__ __forceinline__ Part8 tree_add(const Part8& x, const Part8& y) {
   Part8 z;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    if (COMP) {
-      f2_t e;
-      z.h[u] = f2_two_sum(x.h[u], y.h[u], e);
-      z.l[u] = f2_add(f2_add(x.l[u], e), y.l[u]);
-    } else {
-      z.h[u] = f2_add(x.h[u], y.h[u]);
-      z.l[u] = 0ull;
-    }
-  }
+  for (int u = 0; u < 4; ++u) z.h[u] = f2_add(x.h[u], y.h[u]);
   return z;
 }
 
@@ -95,32 +83,22 @@ struct StagePos {
 };
 
 // Fold input HH of a stage (4 words = 8 bf16 of this thread) into rank r's partial sum `cur` (kfirst: its first
-// micro-step; compensated: Knuth TwoSum with the error terms in cur.l).  At the rank's last micro-step (klast) the
-// rank is complete: the slots below the lowest clear bit of r are all occupied and merge into it, and that
-// bit's slot takes the sum (static slot indices keep every slot in registers).  When r completes a block of
-// 2^LEVELS ranks, cur is left holding the total.
-template <bool COMP, int LEVELS, int HH, int NW>
+// micro-step).  At the rank's last micro-step (klast) the rank is complete: the slots below the lowest clear
+// bit of r are all occupied and merge into it, and that bit's slot takes the sum (static slot indices keep
+// every slot in registers).  When r completes a block of 2^LEVELS ranks, cur is left holding the total.
+template <int LEVELS, int HH, int NW>
 __device__ __forceinline__ void tree_fold(Part8 (&slot)[LEVELS], Part8& cur, const uint32_t (&w)[NW], int r,
                                           bool kfirst, bool klast) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const f2_t xx = bf16x2_to_f2(w[4 * HH + u]);
-    if (kfirst) {
-      cur.h[u] = xx;
-      cur.l[u] = 0ull;
-    } else if (COMP) {
-      f2_t e;
-      cur.h[u] = f2_two_sum(cur.h[u], xx, e);
-      cur.l[u] = f2_add(cur.l[u], e);
-    } else {
-      cur.h[u] = f2_add(cur.h[u], xx);
-    }
+    cur.h[u] = kfirst ? xx : f2_add(cur.h[u], xx);
   }
   if (klast) {
     const int top = __ffs(~r) - 1;
 #pragma unroll
     for (int lv = 0; lv < LEVELS; ++lv) {
-      if (lv < top) cur = tree_add<COMP>(slot[lv], cur);
+      if (lv < top) cur = tree_add(slot[lv], cur);
       else if (lv == top) slot[lv] = cur;
     }
   }
@@ -143,10 +121,10 @@ __device__ __forceinline__ Half half_of(const Tile& t, int h) {
 
 // LEVELS = log2 of the largest n this instance serves (3: n <= 8, 4: n <= 16); slots 0..LEVELS-1 hold
 // pending blocks, and a full block of 2^LEVELS ranks is the total itself.
-template <int MAXSEG, bool COMP, int LEVELS>
+template <int MAXSEG, int LEVELS>
 __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid_constant__ TreeParams<MAXSEG> p) {
-  constexpr int NPS = tt_nps<LEVELS, COMP>();
-  constexpr int NST = tt_stages<LEVELS, COMP>();
+  constexpr int NPS = TT_NPS;
+  constexpr int NST = TT_STAGES;
   constexpr int SBY = NPS * TT_IN_BYTES;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
@@ -243,7 +221,7 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
         // One stage: wait for its bytes, take this thread's 8 values of each of its cnt inputs (input q0 + hh),
         // release the slot.  whole (a whole half tile below the buffer's last partial 8-group): shared loads
         // only.  Otherwise inactive threads take zeros and the tail group is read from global memory.
-        auto take = [&](bool whole, int cnt, int q0, uint32_t (&w)[4 * tt_nps<LEVELS, COMP>()]) {
+        auto take = [&](bool whole, int cnt, int q0, uint32_t (&w)[4 * TT_NPS]) {
           if (live && !mbar_wait_bounded(smem_u32(&full[sp.slot]), sp.phase, p.timeout_ns, s_abort)) {
             if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
             *s_abort = 1;
@@ -297,18 +275,18 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
           const int cnt = nin - q < NPS ? nin - q : NPS;
           uint32_t w[4 * NPS];
           take(whole_half, cnt, q, w);
-          tree_fold<COMP, LEVELS, 0>(slot, cur, w, r, k == 0, k == a - 1);
+          tree_fold<LEVELS, 0>(slot, cur, w, r, k == 0, k == a - 1);
           if (++k == a) { k = 0; ++r; }
           if (NPS > 1 && cnt > 1) {
-            tree_fold<COMP, LEVELS, H1>(slot, cur, w, r, k == 0, k == a - 1);
+            tree_fold<LEVELS, H1>(slot, cur, w, r, k == 0, k == a - 1);
             if (++k == a) { k = 0; ++r; }
           }
           if (NPS > 2 && cnt > 2) {
-            tree_fold<COMP, LEVELS, H2>(slot, cur, w, r, k == 0, k == a - 1);
+            tree_fold<LEVELS, H2>(slot, cur, w, r, k == 0, k == a - 1);
             if (++k == a) { k = 0; ++r; }
           }
           if (NPS > 3 && cnt > 3) {
-            tree_fold<COMP, LEVELS, H3>(slot, cur, w, r, k == 0, k == a - 1);
+            tree_fold<LEVELS, H3>(slot, cur, w, r, k == 0, k == a - 1);
             if (++k == a) { k = 0; ++r; }
           }
           q += cnt;
@@ -322,7 +300,7 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
 #pragma unroll
           for (int lv = 0; lv < LEVELS; ++lv) {
             if ((n >> lv) & 1) {
-              tot = have ? tree_add<COMP>(slot[lv], tot) : slot[lv];
+              tot = have ? tree_add(slot[lv], tot) : slot[lv];
               have = true;
             }
           }
@@ -330,8 +308,7 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
         float o[TT_EPT];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const f2_t pp = COMP ? f2_add(tot.h[u], tot.l[u]) : tot.h[u];
-          f2_unpack(f2_mul(pp, inv2), o[2 * u], o[2 * u + 1]);
+          f2_unpack(f2_mul(tot.h[u], inv2), o[2 * u], o[2 * u + 1]);
         }
         if (active) {
           float* dst = p.gbar[t.owner] + (t.loff + (e0 - t.goff));
@@ -366,33 +343,41 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_kernel(const __grid
                      p.merge);
 }
 
-// ---------------------------------------------------------------- compensated, n <= 8: rank-major stages
+// ---------------------------------------------------------------- compensated: rank-major stages
 //
-// reduce_tree_rm_kernel: the compensated tree for a compile-time rank count N <= 8.  A stage holds micro-step k
-// of every rank for one sub-tile (N bulk copies on one barrier).  Each consumer thread carries the N ranks'
-// (hi, lo) leaf sums of its EPT elements across the micro-steps -- N * EPT / 2 independent packed lanes, where
-// the binary counter above has EPT / 2 -- and after the last micro-step adds the leaves up the binomial tree
-// level by level, every merge fixed at compile time: no pending slots and no rank-dependent branches.  Each
-// leaf is the same chain and each merge the same operation on the same operands as in the binary counter, so
-// the result is the same bits.  EPT * N = 32 for N >= 2: a stage is 30 KB or less, and the leaves take 64
-// registers a thread at most.
+// reduce_tree_rm_kernel: the compensated tree for a compile-time rank count N.  The ranks go in groups of at
+// most eight: [0, min(N, 8)) and, for N > 8, [8, N).  A stage holds micro-step k of every rank of a group for
+// one sub-tile (one bulk copy per rank on one barrier, issued by as many producer lanes).  Each consumer
+// thread carries the group's (hi, lo) leaf sums of its EPT elements across the micro-steps -- NG * EPT / 2
+// independent packed lanes -- and after the last micro-step adds them up the group's binomial tree level by
+// level, every merge fixed at compile time.  For N > 8 the two groups' totals then merge once, block [0, 8) on
+// the left: the binomial tree restricted to ranks [8, N) is the tree of N - 8 ranks shifted by 8 (levels 0-2
+// pair ranks only inside aligned blocks of eight), and its level 3 is that one merge.  Each leaf is the same
+// chain and each merge the same operation on the same operands as in the tree's definition, so the result is
+// the same bits.  EPT = 16, 8, 4 for groups of <= 2, <= 4, <= 8 ranks: a stage is 30 KB or less, and the leaves
+// take 64 registers a thread at most.
 constexpr int RM_MAX_STAGES = 12;
+constexpr int RM_GROUP = 8;
 template <int N>
-__host__ __device__ constexpr int rm_ept() { return N <= 2 ? 16 : (N <= 4 ? 8 : 4); }
+__host__ __device__ constexpr int rm_g1() { return N < RM_GROUP ? N : RM_GROUP; }   // ranks of the first group
+template <int N>
+__host__ __device__ constexpr int rm_ept() { return rm_g1<N>() <= 2 ? 16 : (rm_g1<N>() <= 4 ? 8 : 4); }
 template <int N>
 __host__ __device__ constexpr int rm_sub() { return TT_CTHREADS * rm_ept<N>(); }      // elements of a sub-tile
 template <int N>
 __host__ __device__ constexpr int rm_in_bytes() { return 2 * rm_sub<N>(); }         // one input's sub-tile
 template <int N>
+__host__ __device__ constexpr int rm_stage_bytes() { return rm_g1<N>() * rm_in_bytes<N>(); }
+template <int N>
 __host__ __device__ constexpr int rm_stages() {
-  return TT_RING_BYTES / (N * rm_in_bytes<N>()) < RM_MAX_STAGES ? TT_RING_BYTES / (N * rm_in_bytes<N>())
-                                                                : RM_MAX_STAGES;
+  return TT_RING_BYTES / rm_stage_bytes<N>() < RM_MAX_STAGES ? TT_RING_BYTES / rm_stage_bytes<N>() : RM_MAX_STAGES;
 }
-static_assert(RM_MAX_STAGES <= TT_MAX_STAGES, "the barriers fit the tree kernel's shared layout");
+static_assert(RM_MAX_STAGES <= TT_MAX_STAGES, "the barriers fit the shared layout");
 static_assert(TILE % rm_sub<8>() == 0 && TILE % rm_sub<4>() == 0 && TILE % rm_sub<2>() == 0,
               "a tile is a whole number of sub-tiles");
 static_assert(rm_sub<8>() % 8 == 0 && rm_in_bytes<8>() % 16 == 0, "sub-tiles start on 16-byte boundaries");
-static_assert(rm_stages<8>() >= 4 && rm_stages<7>() >= 4, "at least four stages in flight");
+static_assert(rm_stages<16>() >= 4 && rm_stages<8>() >= 4 && rm_stages<7>() >= 4, "at least four stages in flight");
+static_assert(DP_MAX_N <= 2 * RM_GROUP, "two groups cover every rank count");
 
 // The range of sub-tile h (SUB elements) of a tile, copied as the 8-aligned hull (as half_of).
 __device__ __forceinline__ Half sub_of(const Tile& t, int h, int sub) {
@@ -419,12 +404,12 @@ __device__ __forceinline__ void rm_load(const unsigned char* s, uint32_t (&w)[EP
   }
 }
 
-// One micro-step of every rank into the leaves: the first sets (h, l) = (x, 0), later ones
+// One micro-step of every rank of a group into its leaves: the first sets (h, l) = (x, 0), later ones
 // (h, e) = TwoSum(h, x), l = l + e.
-template <int N, int W, bool FIRST>
-__device__ __forceinline__ void rm_fold(f2_t (&h)[N][W], f2_t (&l)[N][W], const uint32_t (&w)[N][W]) {
+template <int NG, int W, bool FIRST>
+__device__ __forceinline__ void rm_fold(f2_t (&h)[NG][W], f2_t (&l)[NG][W], const uint32_t (&w)[NG][W]) {
 #pragma unroll
-  for (int r = 0; r < N; ++r)
+  for (int r = 0; r < NG; ++r)
 #pragma unroll
     for (int u = 0; u < W; ++u) {
       const f2_t x = bf16x2_to_f2(w[r][u]);
@@ -439,35 +424,44 @@ __device__ __forceinline__ void rm_fold(f2_t (&h)[N][W], f2_t (&l)[N][W], const 
     }
 }
 
-// One level of the binomial tree over the leaves: block r (a multiple of 2 STEP) takes block r + STEP on its
-// right, (H, e) = TwoSum(H_r, H_right), L = (L_r + e) + L_right; a block with no partner stays.
-template <int N, int W, int STEP>
-__device__ __forceinline__ void rm_level(f2_t (&h)[N][W], f2_t (&l)[N][W]) {
+// left + right on W packed lanes, the lower-index block on the left: (H, e) = TwoSum(H_left, H_right),
+// L = (L_left + e) + L_right.
+template <int W>
+__device__ __forceinline__ void rm_merge(f2_t (&hl)[W], f2_t (&ll)[W], const f2_t (&hr)[W], const f2_t (&lr)[W]) {
 #pragma unroll
-  for (int r = 0; r + STEP < N; r += 2 * STEP)
-#pragma unroll
-    for (int u = 0; u < W; ++u) {
-      f2_t e;
-      const f2_t H = f2_two_sum(h[r][u], h[r + STEP][u], e);
-      l[r][u] = f2_add(f2_add(l[r][u], e), l[r + STEP][u]);
-      h[r][u] = H;
-    }
+  for (int u = 0; u < W; ++u) {
+    f2_t e;
+    const f2_t H = f2_two_sum(hl[u], hr[u], e);
+    ll[u] = f2_add(f2_add(ll[u], e), lr[u]);
+    hl[u] = H;
+  }
 }
-// The whole tree, levels 0, 1, 2 in turn; the total is left in leaf 0.
-template <int N, int W>
-__device__ __forceinline__ void rm_tree(f2_t (&h)[N][W], f2_t (&l)[N][W]) {
-  if constexpr (N > 1) rm_level<N, W, 1>(h, l);
-  if constexpr (N > 2) rm_level<N, W, 2>(h, l);
-  if constexpr (N > 4) rm_level<N, W, 4>(h, l);
+
+// One level of the binomial tree over a group's leaves: block r (a multiple of 2 STEP) takes block r + STEP on
+// its right; a block with no partner stays.
+template <int NG, int W, int STEP>
+__device__ __forceinline__ void rm_level(f2_t (&h)[NG][W], f2_t (&l)[NG][W]) {
+#pragma unroll
+  for (int r = 0; r + STEP < NG; r += 2 * STEP) rm_merge<W>(h[r], l[r], h[r + STEP], l[r + STEP]);
+}
+// The group's whole tree, levels 0, 1, 2 in turn; the total is left in leaf 0.
+template <int NG, int W>
+__device__ __forceinline__ void rm_tree(f2_t (&h)[NG][W], f2_t (&l)[NG][W]) {
+  static_assert(NG <= RM_GROUP, "a group has at most eight ranks");
+  if constexpr (NG > 1) rm_level<NG, W, 1>(h, l);
+  if constexpr (NG > 2) rm_level<NG, W, 2>(h, l);
+  if constexpr (NG > 4) rm_level<NG, W, 4>(h, l);
 }
 
 template <int MAXSEG, int N>
 __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __grid_constant__ TreeParams<MAXSEG> p) {
+  constexpr int G1 = rm_g1<N>();               // ranks [0, G1)
+  constexpr int G2 = N - G1;                   // ranks [8, N), none for N <= 8
   constexpr int EPT = rm_ept<N>();
   constexpr int W = EPT / 2;
   constexpr int SUB = rm_sub<N>();
   constexpr int IN = rm_in_bytes<N>();
-  constexpr int SBY = N * IN;
+  constexpr int SBY = rm_stage_bytes<N>();
   constexpr int NST = rm_stages<N>();
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* stages = smem;
@@ -508,45 +502,58 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
 
   unsigned bad = 0;
   if (warp == TT_CWARPS) {
-    // ------------------------------------------------------------ producer: per sub-tile, micro-step k of every rank
-    if (lane == 0) {
-      StagePos<NST> sp;
-      TileWalker<MAXSEG> walk;
-      for (int tile = blockIdx.x; tile < ntiles && !*s_abort; tile += gridDim.x) {
-        const Tile t = walk.at(p.seg, tile);
-        for (int h = 0; h < TILE / SUB && !*s_abort; ++h) {
-          const Half x = sub_of(t, h, SUB);
-          if (x.empty()) continue;
-          int64_t sb = (x.hi + 7) & ~int64_t(7);
-          if (sb > p8) sb = p8;
-          const uint32_t bytes = sb > x.sa ? (uint32_t)(sb - x.sa) * 2u : 0u;
-          for (int k = 0; k < a && !*s_abort; ++k) {
-            if (sp.count >= (uint32_t)NST &&
-                !mbar_wait_bounded(smem_u32(&empty[sp.slot]), sp.phase ^ 1u, p.timeout_ns, s_abort)) {
-              if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
-              *s_abort = 1;
+    // ------------------------------------------------------------ producer warp: per sub-tile and group, micro-step
+    // k of the group's ranks.  Lane 0 waits for the slot and posts the byte count; lane r then copies rank r.
+    StagePos<NST> sp;
+    TileWalker<MAXSEG> walk;
+    bool stop = false;
+    for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
+      const Tile t = walk.at(p.seg, tile);
+      for (int h = 0; h < TILE / SUB && !stop; ++h) {
+        const Half x = sub_of(t, h, SUB);
+        if (x.empty()) continue;
+        int64_t sb = (x.hi + 7) & ~int64_t(7);
+        if (sb > p8) sb = p8;
+        const uint32_t bytes = sb > x.sa ? (uint32_t)(sb - x.sa) * 2u : 0u;
+        for (int gq = 0; gq < (G2 > 0 ? 2 : 1) && !stop; ++gq) {
+          const int r0 = gq ? RM_GROUP : 0, ng = gq ? G2 : G1;
+          for (int k = 0; k < a; ++k) {
+            const uint32_t fb = smem_u32(&full[sp.slot]);
+            int ok = 1;
+            if (lane == 0) {
+              if (*s_abort) {
+                ok = 0;
+              } else if (sp.count >= (uint32_t)NST &&
+                         !mbar_wait_bounded(smem_u32(&empty[sp.slot]), sp.phase ^ 1u, p.timeout_ns, s_abort)) {
+                if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+                *s_abort = 1;
+                ok = 0;
+              }
+              if (ok) mbar_arrive_expect_tx(fb, bytes * (uint32_t)ng);
+            }
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            __syncwarp();
+            if (!ok) {
+              stop = true;
               break;
             }
-            const uint32_t fb = smem_u32(&full[sp.slot]);
-            mbar_arrive_expect_tx(fb, bytes * (uint32_t)N);
-            if (bytes)
-              for (int r = 0; r < N; ++r)
-                bulk_g2s(smem_u32(stages + sp.slot * SBY + r * IN), p.g[r * a + k] + x.sa, bytes, fb);
+            if (bytes && lane < ng)
+              bulk_g2s(smem_u32(stages + sp.slot * SBY + lane * IN), p.g[(r0 + lane) * a + k] + x.sa, bytes, fb);
             sp.next();
           }
         }
       }
-      // Never leave with copies in flight: wait for the newest issued phase of every slot.
-      if (*s_abort) {
-        const uint32_t it = sp.count;
-        const uint32_t first = it > (uint32_t)NST ? it - NST : 0u;
-        for (uint32_t y = first; y < it; ++y)
-          (void)mbar_wait_bounded(smem_u32(&full[y % NST]), (y / NST) & 1u, p.timeout_ns, nullptr);
-      }
+    }
+    // Never leave with copies in flight: wait for the newest issued phase of every slot.
+    if (lane == 0 && *s_abort) {
+      const uint32_t it = sp.count;
+      const uint32_t first = it > (uint32_t)NST ? it - NST : 0u;
+      for (uint32_t y = first; y < it; ++y)
+        (void)mbar_wait_bounded(smem_u32(&full[y % NST]), (y / NST) & 1u, p.timeout_ns, nullptr);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ consumers: EPT elements of N ranks per thread
+    // ------------------------------------------------------------ consumers: EPT elements of every rank per thread
     const f2_t inv2 = f2_pack(s_inv, s_inv);
     StagePos<NST> sp;
     TileWalker<MAXSEG> walk;
@@ -560,11 +567,12 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
         const bool active = e0 < x.hi;
         const bool tailgrp = active && (e0 + EPT > p8);
 
-        // One stage (micro-step k): wait for its bytes, take this thread's EPT values of every rank, release the
-        // slot.  WHOLE (a whole sub-tile below the buffer's last partial 8-group): shared loads only.
-        // Otherwise inactive threads take zeros and the tail group is read from global memory.
-        auto take = [&](auto whole_tag, int k, uint32_t (&w)[N][W]) {
+        // One stage (micro-step k of the group from rank r0): wait for its bytes, take this thread's EPT values
+        // of each rank, release the slot.  WHOLE (a whole sub-tile below the buffer's last partial 8-group):
+        // shared loads only.  Otherwise inactive threads take zeros and the tail group is read from global.
+        auto take = [&](auto whole_tag, int r0, int k, auto& w) {
           constexpr bool WHOLE = decltype(whole_tag)::value;
+          constexpr int NG = sizeof(w) / sizeof(w[0]);
           if (live && !mbar_wait_bounded(smem_u32(&full[sp.slot]), sp.phase, p.timeout_ns, s_abort)) {
             if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
             *s_abort = 1;
@@ -573,19 +581,19 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
           const unsigned char* src_s = stages + sp.slot * SBY + 2 * EPT * tid;
           if constexpr (WHOLE) {
 #pragma unroll
-            for (int r = 0; r < N; ++r) rm_load<EPT>(src_s + r * IN, w[r]);
+            for (int r = 0; r < NG; ++r) rm_load<EPT>(src_s + r * IN, w[r]);
           } else {
 #pragma unroll
-            for (int r = 0; r < N; ++r)
+            for (int r = 0; r < NG; ++r)
 #pragma unroll
               for (int u = 0; u < W; ++u) w[r][u] = 0u;
             if (active && live) {
 #pragma unroll
-              for (int r = 0; r < N; ++r) {
+              for (int r = 0; r < NG; ++r) {
                 if (!tailgrp) {
                   rm_load<EPT>(src_s + r * IN, w[r]);
                 } else {
-                  const uint16_t* src = p.g[r * a + k];
+                  const uint16_t* src = p.g[(r0 + r) * a + k];
 #pragma unroll
                   for (int u = 0; u < EPT; ++u) {
                     const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
@@ -602,23 +610,33 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
           sp.next();
         };
 
-        // The leaves over the micro-steps, then the tree.
-        f2_t hs[N][W], ls[N][W];
-        auto run = [&](auto whole_tag) {
+        // A group's leaves over the micro-steps (whole: the sub-tile takes the guard-free loads), then its tree;
+        // for N > 8 the second group's total joins the first's on the right.  The total is left in leaf 0.
+        auto fold_group = [&](auto whole_tag, int r0, auto& hs, auto& ls) {
+          constexpr int NG = sizeof(hs) / sizeof(hs[0]);
           {
-            uint32_t w[N][W];
-            take(whole_tag, 0, w);
-            rm_fold<N, W, true>(hs, ls, w);
+            uint32_t w[NG][W];
+            take(whole_tag, r0, 0, w);
+            rm_fold<NG, W, true>(hs, ls, w);
           }
           for (int k = 1; k < a; ++k) {
-            uint32_t w[N][W];
-            take(whole_tag, k, w);
-            rm_fold<N, W, false>(hs, ls, w);
+            uint32_t w[NG][W];
+            take(whole_tag, r0, k, w);
+            rm_fold<NG, W, false>(hs, ls, w);
           }
         };
-        if (x.hi - x.lo == SUB && x.hi <= p8) run(std::true_type{});
-        else run(std::false_type{});
-        rm_tree<N, W>(hs, ls);
+        const bool whole = x.hi - x.lo == SUB && x.hi <= p8;
+        f2_t hs[G1][W], ls[G1][W];
+        if (whole) fold_group(std::true_type{}, 0, hs, ls);
+        else fold_group(std::false_type{}, 0, hs, ls);
+        rm_tree<G1, W>(hs, ls);
+        if constexpr (G2 > 0) {
+          f2_t hs2[G2][W], ls2[G2][W];
+          if (whole) fold_group(std::true_type{}, RM_GROUP, hs2, ls2);
+          else fold_group(std::false_type{}, RM_GROUP, hs2, ls2);
+          rm_tree<G2, W>(hs2, ls2);
+          rm_merge<W>(hs[0], ls[0], hs2[0], ls2[0]);
+        }
 
         float o[EPT];
 #pragma unroll
@@ -776,8 +794,7 @@ cudaError_t launch_tree_kernel(const TreeParams<MAXSEG>& prm, int ntiles, cudaSt
   return cudaGetLastError();
 }
 
-// Compensated with n <= 8: the rank-major kernel for that n.  Otherwise the binary counter (n <= 8 plain,
-// n <= 16 either arithmetic).
+// Compensated: the rank-major kernel for that n.  Plain: the binary counter.
 template <int MAXSEG, bool COMP>
 cudaError_t launch_tree_n(const Plan& P, const uint16_t* const* g, int a, float* const* gbar,
                           const StepScalars& s, int advance, dp_step_state_t* st, cudaStream_t stream) {
@@ -792,11 +809,19 @@ cudaError_t launch_tree_n(const Plan& P, const uint16_t* const* g, int a, float*
       case 6: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 6>, MAXSEG>(prm, P.ntiles, stream);
       case 7: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 7>, MAXSEG>(prm, P.ntiles, stream);
       case 8: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 8>, MAXSEG>(prm, P.ntiles, stream);
-      default: return launch_tree_kernel<reduce_tree_kernel<MAXSEG, true, 4>, MAXSEG>(prm, P.ntiles, stream);
+      case 9: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 9>, MAXSEG>(prm, P.ntiles, stream);
+      case 10: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 10>, MAXSEG>(prm, P.ntiles, stream);
+      case 11: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 11>, MAXSEG>(prm, P.ntiles, stream);
+      case 12: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 12>, MAXSEG>(prm, P.ntiles, stream);
+      case 13: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 13>, MAXSEG>(prm, P.ntiles, stream);
+      case 14: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 14>, MAXSEG>(prm, P.ntiles, stream);
+      case 15: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 15>, MAXSEG>(prm, P.ntiles, stream);
+      case 16: return launch_tree_kernel<reduce_tree_rm_kernel<MAXSEG, 16>, MAXSEG>(prm, P.ntiles, stream);
+      default: return cudaErrorInvalidValue;
     }
   } else {
-    if (P.n <= 8) return launch_tree_kernel<reduce_tree_kernel<MAXSEG, false, 3>, MAXSEG>(prm, P.ntiles, stream);
-    return launch_tree_kernel<reduce_tree_kernel<MAXSEG, false, 4>, MAXSEG>(prm, P.ntiles, stream);
+    if (P.n <= 8) return launch_tree_kernel<reduce_tree_kernel<MAXSEG, 3>, MAXSEG>(prm, P.ntiles, stream);
+    return launch_tree_kernel<reduce_tree_kernel<MAXSEG, 4>, MAXSEG>(prm, P.ntiles, stream);
   }
 }
 
