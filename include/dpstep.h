@@ -527,8 +527,7 @@ dp_status_t dp_selftest_wait_timeout(dp_step_state_t* d_state, uint64_t timeout_
  * launched.  Arguments, results and errors are those of dp_step; no call
  * allocates or frees memory.  Every call looks up the array's device address
  * in the current context (cudaGetSymbolAddress; the first call on a device
- * also loads the library's kernels there) -- make the first call on a device
- * before any stream capture on that device.  All calls share the array and it
+ * also loads the library's kernels there).  All calls share the array and it
  * keeps the last call's contents; calls whose kernels overlap on the GPU race
  * on it, so order them (one stream, or events). */
 dp_status_t dp_step_static(uint16_t* const* replicas, float* const* master, float* const* m, float* const* v,
