@@ -8,8 +8,8 @@
 // of two) goes up a level unchanged.  The order does not depend on the shard owner (the all-reduce root is
 // rank 0 for every element); each owner keeps its shard of the result.
 //
-// Both pass-A kernels take the ring kernel's stream: one producer thread issuing 1-D bulk copies into a ring
-// of shared-memory stages, bounded mbarrier waits.
+// Both pass-A kernels take the ring kernel's stream: a producer warp issuing 1-D bulk copies into a ring of
+// shared-memory stages, bounded mbarrier waits.
 // reduce_tree_kernel (plain arithmetic): consumers keep the tree as a binary counter -- slot l holds the
 // pending sum of a complete block of 2^l ranks, so at most log2(n) partial sums are live, each in registers.
 // A consumer thread owns 8 elements (the ring kernel's 16), so a stage input is half a tile (3840 elements, a
@@ -104,8 +104,9 @@ __device__ __forceinline__ void tree_fold(Part8 (&slot)[LEVELS], Part8& cur, con
   }
 }
 
-// The stage range of half h of a tile: the tile's elements [lo, hi) in that half, copied as the 8-aligned
-// hull [lo & ~7, min(ceil8(hi), psi & ~7)) -- the buffer's last partial 8 elements are read from global.
+// The elements [lo, hi) of a tile inside one part of its cell (a half tile here, a sub-tile below), copied as
+// the 8-aligned hull [lo & ~7, min(ceil8(hi), psi & ~7)) -- the buffer's last partial 8 elements are read
+// from global memory.
 struct Half {
   int64_t lo, hi, sa;
   __device__ __forceinline__ bool empty() const { return lo >= hi; }
