@@ -14,7 +14,8 @@ path; hbm_gbs_path_bytes counts the bytes the timed path's own design moves (B1 
 The end-to-end leg ("e2e") times the same step through one C-ABI call with the gradients in host memory
 (dp_step_single_pass_from_host, or dp_step_from_host for --path two-pass): every step's gradients copied from
 pinned host memory, the step, and the 64-byte step state read back.  --order tree times the binomial-tree order
-(two-pass path); --workload also takes the flat sweep's case names (sweep_<psi>_n<n>_a<a>_<even|ragged>).
+(on the single pass, or with --path two-pass on dp_step); --workload also takes the flat sweep's case names
+(sweep_<psi>_n<n>_a<a>_<even|ragged>).
 
 Multi-GPU (torchrun): every rank holds one workload-sized slice of an N-times-larger parameter space (weak
 scaling) and runs the sliced step: its reduction with the commit deferred, one 4-byte NCCL all-reduce (MAX) of
@@ -62,13 +63,12 @@ def parse():
                    help="order of the ranks' sums: the ring reduce-scatter's, or a binomial tree's")
     p.add_argument("--path", choices=["two-pass", "single-pass", "microstep"], default=None,
                    help="dp_step_single_pass (one pass, two state sets; the default), dp_step (reduce + update "
-                        "kernels; the default with --order tree) or dp_reduce_scatter_micro per micro-step + "
-                        "dp_step_update (the ZeRO-2 form)")
+                        "kernels) or dp_reduce_scatter_micro per micro-step + dp_step_update (the ZeRO-2 form)")
     p.add_argument("--stage", type=int, default=-1, choices=[-1, 0, 1, 2, 3],
                    help="override the workload's ZeRO stage (0: plain data parallelism, two-pass path)")
     args = p.parse_args()
     if args.path is None:
-        args.path = "two-pass" if args.order == "tree" or args.stage == 0 else "single-pass"
+        args.path = "two-pass" if args.stage == 0 else "single-pass"
     return args
 
 
@@ -123,9 +123,10 @@ def step_bytes(wl):
     return b1, b1 + 8, 2 * wl.n * wl.a + 4, 4 + 24 + 2 * wl.n
 
 
-KERNEL_SOURCES = {"reduce": ("dp_kernels.cu", "dp_device.cuh", "dp_launch.h"),
-                  "update": ("dp_kernels.cu", "dp_device.cuh", "dp_launch.h"),
-                  "single_pass": ("dp_kernels.cu", "dp_device.cuh", "dp_launch.h"),
+KERNEL_SOURCES = {"reduce": ("dp_kernels.cu", "dp_single.cuh", "dp_device.cuh", "dp_launch.h"),
+                  "update": ("dp_kernels.cu", "dp_single.cuh", "dp_device.cuh", "dp_launch.h"),
+                  "single_pass": ("dp_kernels.cu", "dp_single.cuh", "dp_device.cuh", "dp_launch.h"),
+                  "single_pass_tree": ("dp_tree_sp.cu", "dp_single.cuh", "dp_device.cuh", "dp_launch.h"),
                   "reduce_tree": ("dp_tree.cu", "dp_device.cuh", "dp_launch.h"),
                   "rs_micro": ("dp_micro.cu", "dp_device.cuh", "dp_launch.h")}
 
@@ -346,8 +347,6 @@ def native_main(args, wl):
     mode = dp.DP_SUM_COMPENSATED if args.sum == "compensated" else dp.DP_SUM_PLAIN
     tree = args.order == "tree"
     if tree:
-        if args.path == "single-pass":
-            raise SystemExit("--order tree runs on the two-pass path only")
         mode |= dp.DP_ORDER_TREE
     segs = synth.layout_of(wl)
     layout = dp.Layout(wl.stage, wl.n, wl.psi, segs)
@@ -455,8 +454,8 @@ def native_main(args, wl):
     path_bytes = b1 if single else (red_bytes + upd_bytes) if micro else b2
     step_gbs = b1 * wl.psi / (ms * 1e-3) / 1e9           # the single-pass algorithmic minimum, every path
     path_gbs = path_bytes * wl.psi / (ms * 1e-3) / 1e9    # what the timed path's own design moves
-    traffic = recorded_traffic(wl.name, "single_pass" if single else "rs_micro" if micro else
-                               ("reduce_tree" if tree else "reduce"))
+    traffic = recorded_traffic(wl.name, ("single_pass_tree" if tree else "single_pass") if single else
+                               "rs_micro" if micro else ("reduce_tree" if tree else "reduce"))
 
     # End to end through the public call with host buffers: the step's gradients copied from pinned host
     # memory, the step, and the step's status read back, every step -- one C-ABI call does all three
@@ -535,7 +534,8 @@ def native_main(args, wl):
             "split": ({"slices": ws, "collective": "4-byte NCCL all-reduce (MAX) of found_inf per step"}
                       if split else None),
             "roofline": {"bound": "hbm",
-                         "kernel": ("single-pass reduce + Adam + all-gather" if single else
+                         "kernel": ("single-pass reduce (tree order) + Adam + all-gather" if single and tree else
+                                    "single-pass reduce + Adam + all-gather" if single else
                                     "per-micro-step reduce-scatter (a launches per step, summed)" if micro else
                                     "reduce (accumulate + tree reduce + average + check)" if tree else
                                     "reduce (accumulate + ring reduce-scatter + average + check)"),

@@ -95,7 +95,9 @@ enum {
  *     two) moves up a level unchanged.  Compensated: (H, e) = TwoSum(H_left,
  *     H_right), L = (L_left + e) + L_right.  (NCCL's tree algorithms, named on
  *     the same page beside the ring for their 2 log2(n) instead of 2(n-1)
- *     steps.)  dp_step_single_pass takes the ring order only. */
+ *     steps.)  dp_step, dp_step_reduce, dp_step_single_pass and the staged
+ *     reduce-scatter take either order; dp_reduce_scatter_micro the ring
+ *     order only. */
 enum { DP_ORDER_RING = 0, DP_ORDER_TREE = 16 };
 
 /* Step flags, OR'd into sum_mode, for a step split across several GPUs, each
@@ -459,7 +461,8 @@ dp_status_t dp_step_scaled(uint16_t* const* replicas, float* const* master, floa
  * kernel rewrites them as bf16_rne of the (unchanged) current master, so a
  * skipped step leaves the replicas as they were provided they held
  * bf16_rne(master) before it -- the invariant every applied step
- * establishes.  Results are bit-identical to dp_step.  Stages 1-3 only.
+ * establishes.  Results are bit-identical to dp_step in the same order (ring
+ * or DP_ORDER_TREE).  Stages 1-3 only.
  * Accepts DP_DEFER_COMMIT (then only the pass is launched; the state set is
  * not flipped and the replicas not repaired until dp_commit_single_pass) and
  * DP_DEVICE_SCALE in sum_mode. */

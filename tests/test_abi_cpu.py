@@ -306,6 +306,6 @@ def test_single_pass_from_host_argument_errors_queue_nothing(dp):
     assert f(fake, st4, st4, st4, fake, two(16, 17), 1, ctypes.byref(L.c), A, 1.0, 0, 256, None,
              None) == dp.DP_ERR_ALIGNMENT
     assert f(fake, st4, st4, st4, fake, fake, 1, ctypes.byref(L.c), A, 1.0, 0, None, None, None) == dp.DP_ERR_INVALID_ARG
-    assert f(fake, st4, st4, st4, fake, fake, 1, ctypes.byref(L.c), A, 1.0, dp.DP_ORDER_TREE, 256, None,
+    assert f(fake, st4, st4, st4, fake, fake, 1, ctypes.byref(L.c), A, 1.0, dp.DP_ORDER_TREE | (1 << 10), 256, None,
              None) == dp.DP_ERR_INVALID_ARG
     assert dp.dp_kernel_launches() == before

@@ -141,6 +141,12 @@ def test_fullsize_gpt2_small_single_pass(dev):
     run_fullsize(synth.WORKLOADS["gpt2_small"], inject=True, single=True)
 
 
+def test_fullsize_gpt2_small_single_pass_tree_order(dev):
+    """The benchmark's workload through dp_step_single_pass in tree order, and a skipped step after it."""
+    run_fullsize(synth.WORKLOADS["gpt2_small"], inject=True, single=True,
+                 mode=dp.DP_SUM_COMPENSATED | dp.DP_ORDER_TREE)
+
+
 def test_fullsize_gpt_1p3b_single_pass(dev):
     """The 1.3B list's +3-misaligned 25M-bucket ZeRO-3 layout through the single pass, warm m/v."""
     run_fullsize(synth.WORKLOADS["gpt_1p3b"], warm=True, single=True)

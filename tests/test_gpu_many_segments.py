@@ -9,8 +9,8 @@ and only the last commits.  Checked on every launch path:
     not depend on how the segments are grouped into launches), and every path matches the float64 oracle;
   - a non-finite value in the first, a middle or the last run of segments skips the whole step with the exact
     count, t unchanged and every byte of state unchanged;
-  - the single pass, the tree order, the per-micro-step reduce-scatter and the staged calls agree with the
-    oracle on the same layouts.
+  - the single pass (ring and tree order), the two-pass tree order, the per-micro-step reduce-scatter and the
+    staged calls agree with the oracle on the same layouts.
 """
 import numpy as np
 import pytest
@@ -54,19 +54,19 @@ def test_ring_order_and_oracle_over_launches(dev, psi, n, a, stage, extra):
     gu.assert_matches_oracle(gu.gpu_result(c, b), gu.run_oracle(c))
 
 
-@pytest.mark.parametrize("path", ["two_pass", "tree", "single_pass", "microstep", "staged"])
+@pytest.mark.parametrize("path", ["two_pass", "tree", "single_pass", "single_pass_tree", "microstep", "staged"])
 @pytest.mark.parametrize("psi,n,a,stage,extra", LAYOUTS)
 def test_every_path_matches_the_oracle(dev, psi, n, a, stage, extra, path):
     wl, c = case_of(psi, n, a, stage, extra, seed=72)
     A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
-    b = gu.upload(c, second_set=path == "single_pass", micro_acc=path == "microstep")
+    b = gu.upload(c, second_set=path.startswith("single_pass"), micro_acc=path == "microstep")
     S = wl.loss_scale
     if path == "two_pass":
         b.step(A, S)
     elif path == "tree":
         b.step(A, S, dp.DP_SUM_COMPENSATED | dp.DP_ORDER_TREE)
-    elif path == "single_pass":
-        b.step_single_pass(A, S)
+    elif path.startswith("single_pass"):
+        b.step_single_pass(A, S, dp.DP_SUM_COMPENSATED | (dp.DP_ORDER_TREE if path.endswith("tree") else 0))
         b.master, b.m, b.v = b.current()
     elif path == "microstep":
         b.step_micro(A, S)

@@ -6,8 +6,8 @@ combined over the slices with a maximum (here a max over the slices' state words
 in for the 4-byte all-reduce between GPUs), then the commit and the update.  The per-element arithmetic does
 not depend on the slicing, so over three steps -- the second with a non-finite value in the last slice only --
 the slices' results put back together must equal the whole-space step bit for bit: the same t, skip flag,
-master/m/v, replicas (and, with the device-resident loss scale, the same scale).  Two-pass and single-pass
-steps, fixed and dynamic loss scale.
+master/m/v, replicas (and, with the device-resident loss scale, the same scale).  Two-pass steps in ring and
+tree order, single-pass steps, fixed and dynamic loss scale.
 """
 import pytest
 import torch
@@ -83,11 +83,12 @@ def assert_slices_equal_whole(whole, parts, L, single):
 
 
 @pytest.mark.parametrize("scaled", [False, True])
-@pytest.mark.parametrize("single", [False, True])
+@pytest.mark.parametrize("single,order", [(False, 0), (True, 0), (False, dp.DP_ORDER_TREE), (True, dp.DP_ORDER_TREE)])
 @pytest.mark.parametrize("psi,n,a,stage,layout,extra,G", CASES)
-def test_slices_equal_whole_space_step(dev, psi, n, a, stage, layout, extra, G, single, scaled):
+def test_slices_equal_whole_space_step(dev, psi, n, a, stage, layout, extra, G, single, order, scaled):
     if single and stage == 0:
         pytest.skip("the single pass takes stages 1-3")
+    mode = dp.DP_SUM_COMPENSATED | order
     wl = BASE.with_(psi=psi, n=n, a=a, stage=stage, layout=layout, seed=500 + psi % 97, loss_scale=2.0 ** 10,
                     **extra)
     c = gu.make_case(wl)
@@ -121,17 +122,17 @@ def test_slices_equal_whole_space_step(dev, psi, n, a, stage, layout, extra, G, 
             b.grad(n - 1, a - 1)[i:i + 1].view(torch.int16).fill_(val)
         # the whole space in one call
         if scaled and single:
-            whole.step_single_pass(A, 1.0, dp.DP_SUM_COMPENSATED | dp.DP_DEFER_COMMIT | dp.DP_DEVICE_SCALE)
+            whole.step_single_pass(A, 1.0, mode | dp.DP_DEFER_COMMIT | dp.DP_DEVICE_SCALE)
             dp.dp_commit_single_pass(whole.replicas, whole.master + whole.master1, c.layout, A, whole.state, sc)
         elif scaled:
-            whole.step_scaled(A, sc)
+            whole.step_scaled(A, sc, mode)
         elif single:
-            whole.step_single_pass(A, wl.loss_scale)
+            whole.step_single_pass(A, wl.loss_scale, mode)
         else:
-            whole.step(A, wl.loss_scale)
+            whole.step(A, wl.loss_scale, mode)
         # the slices: reduce each with the commit deferred, combine the flags, commit and update each
         for b, *_ in parts:
-            sliced.reduce_deferred(b, A, wl.loss_scale, single_pass=single, scaler_=sc)
+            sliced.reduce_deferred(b, A, wl.loss_scale, mode, single_pass=single, scaler_=sc)
         flags = [ops.found_flag(b) for b, *_ in parts]
         f = torch.stack(flags).max()
         for x in flags:

@@ -4,8 +4,10 @@ compute-sanitizer is not available to these tests, so out-of-bounds stores are l
 buffer a step touches (gradients, replicas, master/m/v and the single pass's second set, gbar shards, the
 per-micro-step accumulators, the step state) sits inside an allocation with 256 sentinel bytes on each side,
 and the bands are checked after every step.  Sizes psi = 1 ... 67 with n in {1, 2, 3, 5, 8} and a in {1, 2, 3}
-run through the four launch paths -- dp_step in ring order and in tree order, dp_step_single_pass, and the
-per-micro-step reduce-scatter + dp_step_update -- and every element is compared with the float64 oracle.
+run through the five launch paths -- dp_step in ring order and in tree order, dp_step_single_pass in both
+orders, and the per-micro-step reduce-scatter + dp_step_update -- and every element is compared with the
+float64 oracle.  The tree order also runs n in {9, 12, 16}, where its ranks form more than one group of eight
+(two-pass) or four (single pass).
 
 Layouts cycle over four kinds, so the misaligned cases reach the kernels' ragged branches:
   - 3-element-misaligned buckets of about psi / 3 elements and 1-misaligned buckets of 5 elements: shard
@@ -28,7 +30,7 @@ import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 
-PATHS = ["two_pass", "tree", "single_pass", "microstep"]
+PATHS = ["two_pass", "tree", "single_pass", "single_pass_tree", "microstep"]
 NS = [1, 2, 3, 5, 8]
 BASE = synth.WORKLOADS["tiny"]
 
@@ -45,12 +47,13 @@ def layout_kind(i: int, psi: int) -> dict:
 
 
 def run_case(path: str, psi: int, n: int, a: int, i: int) -> None:
-    stage = 1 + i % 3 if path == "single_pass" else i % 4
+    single = path in ("single_pass", "single_pass_tree")
+    stage = 1 + i % 3 if single else i % 4
     wl = BASE.with_(psi=psi, n=n, a=a, stage=stage, seed=9000 + i, loss_scale=float(2 ** (i % 9)),
                     **layout_kind(i, psi))
     c = gu.make_case(wl)
     A = dp.adam(wl.lr, wl.beta1, wl.beta2, wl.eps)
-    b = gu.upload(c, second_set=path == "single_pass", micro_acc=path == "microstep")
+    b = gu.upload(c, second_set=single, micro_acc=path == "microstep")
     guard = gu.Guarded(b)
     S = wl.loss_scale
     if path == "two_pass":
@@ -59,12 +62,14 @@ def run_case(path: str, psi: int, n: int, a: int, i: int) -> None:
         b.step(A, S, dp.DP_SUM_COMPENSATED | dp.DP_ORDER_TREE)
     elif path == "single_pass":
         b.step_single_pass(A, S)
+    elif path == "single_pass_tree":
+        b.step_single_pass(A, S, dp.DP_SUM_COMPENSATED | dp.DP_ORDER_TREE)
     else:
         b.step_micro(A, S)
     torch.cuda.synchronize()
     what = "%s psi=%d n=%d a=%d stage=%d %s" % (path, psi, n, a, stage, wl.layout)
     guard.check(what)
-    if path == "single_pass":
+    if single:
         b.master, b.m, b.v = b.current()
     g = gu.gpu_result(c, b)
     o = gu.run_oracle(c, threads=1)
@@ -77,6 +82,16 @@ def run_case(path: str, psi: int, n: int, a: int, i: int) -> None:
 @pytest.mark.parametrize("n", NS)
 @pytest.mark.parametrize("path", PATHS)
 def test_tiny_sizes_guarded(dev, path, n):
+    i = 0
+    for psi in range(1, 68):
+        for a in (1, 2, 3):
+            run_case(path, psi, n, a, i)
+            i += 1
+
+
+@pytest.mark.parametrize("path", ["tree", "single_pass_tree"])
+@pytest.mark.parametrize("n", [9, 12, 16])
+def test_tiny_sizes_guarded_tree_groups(dev, n, path):
     i = 0
     for psi in range(1, 68):
         for a in (1, 2, 3):

@@ -132,10 +132,95 @@ def test_tree_with_device_loss_scale(dev):
 
 
 def test_tree_rejected_where_unsupported(dev):
-    wl = BASE.with_(psi=5000, n=2, a=1)
+    """The per-micro-step reduce-scatter runs in ring order only, and dp_step takes no deferred commit."""
+    wl = BASE.with_(psi=5000, n=2, a=2)
+    c = gu.make_case(wl)
+    b = gu.upload(c, micro_acc=True)
+    with pytest.raises(dp.DPError):
+        b.step_micro(adam_of(wl), 1.0, COMP | TREE)
+    with pytest.raises(dp.DPError):
+        b.step(adam_of(wl), 1.0, COMP | TREE | dp.DP_DEFER_COMMIT)
+
+
+# ---------------------------------------------------------------- the tree order's single pass
+
+SP_CASES = [
+    # psi, n, a, stage, layout, extra -- every element class (n = 1: 16 elements a thread, n = 2: 8, n >= 3: 4)
+    # and group count (n <= 4: one group of four, up to 16: four)
+    (1, 1, 1, 1, "even", {}),
+    (7, 2, 1, 1, "even", {}),
+    (7680 * 3 + 11, 3, 2, 2, "ragged", {}),
+    (7680 * 5 + 1, 4, 8, 3, "even", {}),
+    (300_007, 5, 3, 2, "random", {"nseg": 200}),
+    (30_000, 6, 1, 1, "random", {"nseg": 30}),
+    (100_003, 8, 4, 1, "even", {}),
+    (100_003, 8, 1, 3, "buckets", {"bucket": 23_456, "misalign": 3}),
+    (50_001, 9, 2, 1, "ragged", {}),
+    (70_001, 12, 3, 2, "buckets", {"bucket": 9_999, "misalign": 1}),
+    (40_961, 13, 2, 3, "even", {}),
+    (65_536, 16, 4, 3, "random", {"nseg": 21}),
+]
+
+
+def snap_current(b):
+    torch.cuda.synchronize()
+    ms, mm, vv = b.current()
+    return [t.detach().cpu().view(torch.uint8).numpy().tobytes() for t in ms + mm + vv + b.replicas]
+
+
+def snap_two_pass(b):
+    torch.cuda.synchronize()
+    return [t.detach().cpu().view(torch.uint8).numpy().tobytes() for t in b.master + b.m + b.v + b.replicas]
+
+
+@pytest.mark.parametrize("arith", [COMP, PLAIN])
+@pytest.mark.parametrize("psi,n,a,stage,layout,extra", SP_CASES)
+def test_tree_single_pass_equals_two_pass_tree(dev, psi, n, a, stage, layout, extra, arith):
+    """dp_step_single_pass in tree order gives exactly dp_step's tree-order results over three steps with new
+    gradients each time: the same gbar feeds the same Adam, so master/m/v (the current set), the replicas and
+    the step state agree bit for bit."""
+    wl = BASE.with_(psi=psi, n=n, a=a, stage=stage, layout=layout, seed=700 + n + psi % 97, sigma_g=1e-3, **extra)
+    c = gu.make_case(wl)
+    A = adam_of(wl)
+    two = gu.upload(c)
+    one = gu.upload(c, second_set=True)
+    for step in range(3):
+        if step:
+            w2 = wl.with_(seed=wl.seed + step)
+            for q in range(n * a):
+                g = sd.bf16_from_bits(synth.grads_bf16(w2, q // a, q % a))
+                two.grads[q].copy_(g)
+                one.grads[q].copy_(g)
+        two.step(A, wl.loss_scale, arith | TREE)
+        one.step_single_pass(A, wl.loss_scale, arith | TREE)
+        assert snap_current(one) == snap_two_pass(two), step
+        s1, s2 = dp.read_state(one.state), dp.read_state(two.state)
+        assert (s1["t"], s1["found_inf"], s1["nonfinite"], s1["error"]) == (s2["t"], s2["found_inf"], s2["nonfinite"],
+                                                                          s2["error"]) == (step + 1, 0, 0, 0)
+        assert s1["cur_set"] == (step + 1) % 2
+
+
+def test_tree_single_pass_matches_oracle(dev):
+    wl = BASE.with_(psi=123_457, n=8, a=2, stage=2, layout="random", nseg=9, seed=12, loss_scale=2.0 ** 12)
     c = gu.make_case(wl)
     b = gu.upload(c, second_set=True)
-    with pytest.raises(dp.DPError):
-        b.step_single_pass(adam_of(wl), 1.0, COMP | TREE)
-    with pytest.raises(dp.DPError):
-        b.step(adam_of(wl), 1.0, COMP | 32)
+    b.step_single_pass(adam_of(wl), wl.loss_scale, COMP | TREE)
+    torch.cuda.synchronize()
+    b.master, b.m, b.v = b.current()
+    gu.assert_matches_oracle(gu.gpu_result(c, b), gu.run_oracle(c))
+
+
+@pytest.mark.parametrize("n", [3, 8, 11])
+def test_tree_single_pass_skip_keeps_state_and_restores_replicas(dev, n):
+    wl = BASE.with_(psi=50_001, n=n, a=2, stage=3, layout="buckets", bucket=9_000, misalign=3, seed=22)
+    c = gu.make_case(wl)
+    A = adam_of(wl)
+    b = gu.upload(c, second_set=True)
+    b.step_single_pass(A, wl.loss_scale, COMP | TREE)    # an applied step: replicas = bf16(master) from here on
+    before = snap_current(b)
+    st0 = dp.read_state(b.state)
+    b.grads[2 * n - 1].view(torch.int16)[12_345] = synth.BF16_NAN
+    b.step_single_pass(A, wl.loss_scale, COMP | TREE)
+    st = dp.read_state(b.state)
+    assert (st["found_inf"], st["nonfinite"], st["t"], st["cur_set"]) == (1, 1, st0["t"], st0["cur_set"])
+    assert snap_current(b) == before

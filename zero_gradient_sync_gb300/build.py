@@ -1,4 +1,4 @@
-"""Build libdpstep.so in-tree with nvcc for sm_103a (two translation units, compiled in parallel)."""
+"""Build libdpstep.so in-tree with nvcc for sm_103a (its translation units compiled in parallel)."""
 import os
 import subprocess
 import sys
@@ -10,8 +10,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdpstep.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["dp_api.cu", "dp_kernels.cu", "dp_static.cu", "dp_checkpoint.cu", "dp_tree.cu", "dp_micro.cu"]
-HEADERS = ["dp_device.cuh", "dp_internal.h", "dp_launch.h"]
+SOURCES = ["dp_api.cu", "dp_kernels.cu", "dp_static.cu", "dp_checkpoint.cu", "dp_tree.cu", "dp_tree_sp.cu",
+           "dp_micro.cu"]
+HEADERS = ["dp_device.cuh", "dp_internal.h", "dp_launch.h", "dp_single.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

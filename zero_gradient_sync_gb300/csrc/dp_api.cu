@@ -692,7 +692,6 @@ dp_status_t single_pass_impl(uint16_t* const* replicas, float* const* master, fl
     return fail(DP_ERR_INVALID_ARG, "a = %d: need 1 <= a and n * a <= %d", a, DP_MAX_NA);
   StepScalars s;
   if ((st = scalars(P, &adam, loss_scale, sum_mode, s, DP_DEFER_COMMIT | DP_DEVICE_SCALE)) != DP_OK) return st;
-  if (s.order != DP_ORDER_RING) return fail(DP_ERR_INVALID_ARG, "dp_step_single_pass: ring order only");
   if ((st = check_full_arrays(P, (const void* const*)grads, P.n * a, "grads")) != DP_OK) return st;
   if ((st = check_full_arrays(P, (const void* const*)replicas, P.n, "replicas")) != DP_OK) return st;
   int64_t lens2[2 * DP_MAX_N];
