@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
         int64_t sb = (x.hi + 7) & ~int64_t(7);
         if (sb > p8) sb = p8;
         const uint32_t bytes = sb > x.sa ? (uint32_t)(sb - x.sa) * 2u : 0u;
+        const bool tail = x.hi > p8;   // the sub-tile holds elements of the buffer's last partial 8-group
         for (int gq = 0; gq < ngroups && !stop; ++gq) {
           const int r0 = gq * MAXG, ng = n - r0 < MAXG ? n - r0 : MAXG;
           for (int k = 0; k < a; ++k) {
@@ -231,7 +232,6 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
                 *s_abort = 1;
                 ok = 0;
               }
-              if (ok) mbar_arrive_expect_tx(fb, bytes * (uint32_t)ng);
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             __syncwarp();
@@ -239,9 +239,26 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
               stop = true;
               break;
             }
+            unsigned char* slot = stages + rp.slot * TS_SLOT;
+            if (tail && lane < ng) {
+              // The buffer's last partial 8-group (zeros past psi), stored by this lane; ordered before the async
+              // proxy's later writes into the slot by the fence, and before the consumers' reads by the arrive.
+              const uint16_t* src = p.g[(r0 + lane) * a + k];
+              uint32_t v[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t lo = p8 + 2 * u < psi ? (uint32_t)src[p8 + 2 * u] : 0u;
+                const uint32_t hi = p8 + 2 * u + 1 < psi ? (uint32_t)src[p8 + 2 * u + 1] : 0u;
+                v[u] = lo | (hi << 16);
+              }
+              *reinterpret_cast<uint4*>(slot + lane * IN + (p8 - x.sa) * 2) = make_uint4(v[0], v[1], v[2], v[3]);
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(fb, bytes * (uint32_t)ng);
+            __syncwarp();
             if (bytes && lane < ng)
-              bulk_g2s(smem_u32(stages + rp.slot * TS_SLOT + lane * IN), p.g[(r0 + lane) * a + k] + x.sa, bytes,
-                       fb);
+              bulk_g2s(smem_u32(slot + lane * IN), p.g[(r0 + lane) * a + k] + x.sa, bytes, fb);
             rp.next();
             if (++sq == state_after) {
               if (lane == 0) sp_issue_state(p, t, s_cur, sit, s_state, s_ragged, sfull, sempty, s_abort);
@@ -275,13 +292,11 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
         if (x.empty()) continue;
         const int64_t e0 = x.sa + EPT * tid;
         const bool active = e0 < x.hi;
-        const bool tailgrp = active && (e0 + EPT > p8);
 
         // One stage (micro-step k of the ng ranks from r0): wait for its bytes, take this thread's EPT values of
-        // each rank, release the slot.  Inactive threads take zeros and the group holding the buffer's last
-        // partial 8 elements is read from global memory.  (One path for every sub-tile: a second, guard-free
-        // path for whole sub-tiles pushed the kernel past its registers.)
-        auto take = [&](int r0, int ng, int k, auto& w) {
+        // each rank, release the slot.  Every value comes from shared memory: the producer stored the buffer's
+        // last partial 8-group there too.  A thread past the sub-tile's end reads bytes it never uses.
+        auto take = [&](int ng, auto& w) {
           if (live && !mbar_wait_bounded(smem_u32(&full[rp.slot]), rp.phase, p.timeout_ns, s_abort)) {
             if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
             *s_abort = 1;
@@ -290,25 +305,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
           const unsigned char* src_s = stages + rp.slot * TS_SLOT + 2 * EPT * tid;
 #pragma unroll
           for (int r = 0; r < MAXG; ++r)
-#pragma unroll
-            for (int u = 0; u < W; ++u) w[r][u] = 0u;
-          if (active && live) {
-#pragma unroll
-            for (int r = 0; r < MAXG; ++r) {
-              if (r < ng) {
-                if (!tailgrp) {
-                  ts_load<EPT>(src_s + r * IN, w[r]);
-                } else {
-                  const uint16_t* src = p.g[(r0 + r) * a + k];
-#pragma unroll
-                  for (int u = 0; u < EPT; ++u) {
-                    const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
-                    w[r][u >> 1] |= (u & 1) ? (b << 16) : b;
-                  }
-                }
-              }
-            }
-          }
+            if (r < ng) ts_load<EPT>(src_s + r * IN, w[r]);
           // The slot is refilled by the async proxy: order this thread's reads of it before that write.
           fence_proxy_async_smem();
           __syncwarp();
@@ -316,15 +313,15 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
           rp.next();
         };
         // A group's leaves over the micro-steps, then its tree; the total is left in leaf 0.
-        auto group = [&](int r0, int ng, auto& hs, auto& ls) {
+        auto group = [&](int ng, auto& hs, auto& ls) {
           {
             uint32_t w[MAXG][W];
-            take(r0, ng, 0, w);
+            take(ng, w);
             ts_fold<COMP, MAXG, W, true>(hs, ls, w, ng);
           }
           for (int k = 1; k < a; ++k) {
             uint32_t w[MAXG][W];
-            take(r0, ng, k, w);
+            take(ng, w);
             ts_fold<COMP, MAXG, W, false>(hs, ls, w, ng);
           }
           ts_tree<COMP, MAXG, W>(hs, ls, ng);
@@ -336,7 +333,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
         f2_t Ah[W], Al[W];
         if constexpr (MAXG < 4) {
           f2_t hs[MAXG][W], ls[MAXG][W];
-          group(0, n, hs, ls);
+          group(n, hs, ls);
 #pragma unroll
           for (int u = 0; u < W; ++u) {
             Ah[u] = hs[0][u];
@@ -347,7 +344,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
           for (int gq = 0; gq < ngroups; ++gq) {
             const int r0 = gq * MAXG, ng = n - r0 < MAXG ? n - r0 : MAXG;
             f2_t hs[MAXG][W], ls[MAXG][W];
-            group(r0, ng, hs, ls);
+            group(ng, hs, ls);
             if (gq == 0 || gq == 2) {
 #pragma unroll
               for (int u = 0; u < W; ++u) {
