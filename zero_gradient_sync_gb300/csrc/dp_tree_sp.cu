@@ -48,7 +48,7 @@ static_assert(ts_in_bytes<4>() % 16 == 0, "sub-tiles start on 16-byte boundaries
 static_assert(DP_MAX_N <= 4 * ts_g<4>(), "four groups of four cover every rank count");
 
 // The elements [lo, hi) of a tile inside sub-tile h of its cell, copied as the 8-aligned hull
-// [lo & ~7, min(ceil8(hi), psi & ~7)); the buffer's last partial 8 elements are read from global memory.
+// [lo & ~7, min(ceil8(hi), psi & ~7)); the producer stores the buffer's last partial 8-group after it.
 struct SubRange {
   int64_t lo, hi, sa;
   __device__ __forceinline__ bool empty() const { return lo >= hi; }
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(RA_THREADS, 1) tree_single_kernel(const __grid
         const int64_t e0 = x.sa + EPT * tid;
         const bool active = e0 < x.hi;
 
-        // One stage (micro-step k of the ng ranks from r0): wait for its bytes, take this thread's EPT values of
+        // One stage (one micro-step of the group's ng ranks): wait for its bytes, take this thread's EPT values of
         // each rank, release the slot.  Every value comes from shared memory: the producer stored the buffer's
         // last partial 8-group there too.  A thread past the sub-tile's end reads bytes it never uses.
         auto take = [&](int ng, auto& w) {
