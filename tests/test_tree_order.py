@@ -1,5 +1,6 @@
 """The tree reduction order on the CPU: the simulated binomial tree pinned to its definition, to hand-written
-sums, to the step counts that motivate it, and the incremental form the kernels use checked against it."""
+sums, to the step counts that motivate it, and the forms the kernels use -- the incremental binary counter and
+the grouped rank-major form -- checked against it."""
 import math
 
 import numpy as np
@@ -44,6 +45,23 @@ def counter_form(n: int) -> str:
     return tot
 
 
+def grouped_form(n: int, group: int) -> str:
+    """The rank-major kernels' form: the ranks in aligned groups of `group` (a power of two), each group summed
+    up its own binomial tree, then the group totals added up the binomial tree over groups -- the two-pass
+    kernel with groups of eight, the single pass with groups of four."""
+    def tree_of(items):
+        val = list(items)
+        step = 1
+        while step < len(val):
+            for r in range(0, len(val), 2 * step):
+                if r + step < len(val):
+                    val[r] = "(%s+%s)" % (val[r], val[r + step])
+            step *= 2
+        return val[0]
+    groups = [tree_of(["g%d" % r for r in range(lo, min(n, lo + group))]) for lo in range(0, n, group)]
+    return tree_of(groups)
+
+
 HAND = {
     1: "g0",
     2: "(g0+g1)",
@@ -68,6 +86,15 @@ def test_tree_matches_definition_and_kernel_form(n):
     assert e == counter_form(n)
     assert sorted(int(x) for x in e.replace("(", " ").replace(")", " ").replace("+", " ").replace("g", " ").split()) \
         == list(range(n))
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("n", range(1, 17))
+def test_grouped_form_is_the_tree(n, group):
+    """Groups aligned to a power of two, each summed up its own tree, then the totals up the tree over groups,
+    parenthesise exactly as the binomial tree: its levels below log2(group) pair ranks only inside an aligned
+    block of `group`, and the levels above pair whole blocks."""
+    assert grouped_form(n, group) == tree_expression(n)
 
 
 @pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 9, 16])
