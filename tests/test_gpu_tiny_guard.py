@@ -6,7 +6,7 @@ per-micro-step accumulators, the step state) sits inside an allocation with 256 
 and the bands are checked after every step.  Sizes psi = 1 ... 67 with n in {1, 2, 3, 5, 8} and a in {1, 2, 3}
 run through the five launch paths -- dp_step in ring order and in tree order, dp_step_single_pass in both
 orders, and the per-micro-step reduce-scatter + dp_step_update -- and every element is compared with the
-float64 oracle.  The tree order also runs n in {9, 12, 16}, where its ranks form more than one group of eight
+float64 oracle.  The tree order also runs n in {9, 10, 12, 16}, where its ranks form more than one group of eight
 (two-pass) or four (single pass).
 
 Layouts cycle over four kinds, so the misaligned cases reach the kernels' ragged branches:
@@ -90,7 +90,7 @@ def test_tiny_sizes_guarded(dev, path, n):
 
 
 @pytest.mark.parametrize("path", ["tree", "single_pass_tree"])
-@pytest.mark.parametrize("n", [9, 12, 16])
+@pytest.mark.parametrize("n", [9, 10, 12, 16])
 def test_tiny_sizes_guarded_tree_groups(dev, n, path):
     i = 0
     for psi in range(1, 68):

@@ -45,6 +45,10 @@ CASES = [
     (3 * 7680 + 961, 9, 1, 1, "ragged", {}),
     (50_001, 12, 2, 2, "buckets", {"bucket": 4_000, "misalign": 3}),
     (30_721, 15, 3, 3, "even", {}),
+    # n = 9, 10: the second group's micro-steps packed eight and four to a stage (a = 7: one partial stage;
+    # a = 6: a full and a partial one)
+    (20_011, 9, 7, 1, "even", {}),
+    (2 * 7680 + 9, 10, 6, 2, "ragged", {}),
 ]
 
 

@@ -458,6 +458,10 @@ template <int MAXSEG, int N>
 __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __grid_constant__ TreeParams<MAXSEG> p) {
   constexpr int G1 = rm_g1<N>();               // ranks [0, G1)
   constexpr int G2 = N - G1;                   // ranks [8, N), none for N <= 8
+  // Micro-steps of the second group a stage carries: 8 / G2 when that group has one or two ranks (n = 9, 10),
+  // so its stages still carry up to eight copies; one otherwise (packing larger groups spilled registers).
+  constexpr int PK = (G2 > 0 && G2 <= 2) ? RM_GROUP / G2 : 1;
+  constexpr int G2A = G2 > 0 ? G2 : 1;             // its array extent
   constexpr int EPT = rm_ept<N>();
   constexpr int W = EPT / 2;
   constexpr int SUB = rm_sub<N>();
@@ -516,9 +520,13 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
         int64_t sb = (x.hi + 7) & ~int64_t(7);
         if (sb > p8) sb = p8;
         const uint32_t bytes = sb > x.sa ? (uint32_t)(sb - x.sa) * 2u : 0u;
+        // The first group one micro-step a stage; the second PK micro-steps a stage, input l of the stage being
+        // rank 8 + l % G2 at micro-step k + l / G2.
         for (int gq = 0; gq < (G2 > 0 ? 2 : 1) && !stop; ++gq) {
-          const int r0 = gq ? RM_GROUP : 0, ng = gq ? G2 : G1;
-          for (int k = 0; k < a; ++k) {
+          const int r0 = gq ? RM_GROUP : 0, ng = gq ? G2 : G1, pk = gq ? PK : 1;
+          for (int k = 0; k < a; k += pk) {
+            const int cnt = a - k < pk ? a - k : pk;
+            const int ncp = ng * cnt;
             const uint32_t fb = smem_u32(&full[sp.slot]);
             int ok = 1;
             if (lane == 0) {
@@ -530,7 +538,7 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
                 *s_abort = 1;
                 ok = 0;
               }
-              if (ok) mbar_arrive_expect_tx(fb, bytes * (uint32_t)ng);
+              if (ok) mbar_arrive_expect_tx(fb, bytes * (uint32_t)ncp);
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             __syncwarp();
@@ -538,8 +546,9 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
               stop = true;
               break;
             }
-            if (bytes && lane < ng)
-              bulk_g2s(smem_u32(stages + sp.slot * SBY + lane * IN), p.g[(r0 + lane) * a + k] + x.sa, bytes, fb);
+            if (bytes && lane < ncp)
+              bulk_g2s(smem_u32(stages + sp.slot * SBY + lane * IN),
+                       p.g[(r0 + lane % ng) * a + k + lane / ng] + x.sa, bytes, fb);
             sp.next();
           }
         }
@@ -626,6 +635,67 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
             rm_fold<NG, W, false>(hs, ls, w);
           }
         };
+        // The second group when packed: a stage holds micro-steps k .. k + cnt - 1 (cnt <= PK) of its G2 ranks,
+        // folded into the leaves in micro-step order.
+        auto take_packed = [&](auto whole_tag, int k, int cnt, auto& w) {
+          constexpr bool WHOLE = decltype(whole_tag)::value;
+          if (live && !mbar_wait_bounded(smem_u32(&full[sp.slot]), sp.phase, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.state, DP_ERR_TIMEOUT);
+            *s_abort = 1;
+            live = false;
+          }
+          const unsigned char* src_s = stages + sp.slot * SBY + 2 * EPT * tid;
+          if constexpr (WHOLE) {
+#pragma unroll
+            for (int kk = 0; kk < PK; ++kk)
+#pragma unroll
+              for (int r = 0; r < G2; ++r) rm_load<EPT>(src_s + (kk * G2 + r) * IN, w[kk][r]);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < PK; ++kk)
+#pragma unroll
+              for (int r = 0; r < G2; ++r)
+#pragma unroll
+                for (int u = 0; u < W; ++u) w[kk][r][u] = 0u;
+            if (active && live) {
+#pragma unroll
+              for (int kk = 0; kk < PK; ++kk) {
+                if (kk < cnt) {
+#pragma unroll
+                  for (int r = 0; r < G2; ++r) {
+                    if (!tailgrp) {
+                      rm_load<EPT>(src_s + (kk * G2 + r) * IN, w[kk][r]);
+                    } else {
+                      const uint16_t* src = p.g[(RM_GROUP + r) * a + k + kk];
+#pragma unroll
+                      for (int u = 0; u < EPT; ++u) {
+                        const uint32_t b = (e0 + u < psi) ? (uint32_t)src[e0 + u] : 0u;
+                        w[kk][r][u >> 1] |= (u & 1) ? (b << 16) : b;
+                      }
+                    }
+                  }
+                }
+              }
+            }
+          }
+          // The slot is refilled by the async proxy: order this thread's reads of it before that write.
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty[sp.slot]));
+          sp.next();
+        };
+        auto fold_packed = [&](auto whole_tag, auto& hs, auto& ls) {
+          for (int k = 0; k < a; k += PK) {
+            const int cnt = a - k < PK ? a - k : PK;
+            uint32_t w[PK][G2A][W];
+            take_packed(whole_tag, k, cnt, w);
+            if (k == 0) rm_fold<G2, W, true>(hs, ls, w[0]);
+            else rm_fold<G2, W, false>(hs, ls, w[0]);
+#pragma unroll
+            for (int kk = 1; kk < PK; ++kk)
+              if (kk < cnt) rm_fold<G2, W, false>(hs, ls, w[kk]);
+          }
+        };
         const bool whole = x.hi - x.lo == SUB && x.hi <= p8;
         f2_t hs[G1][W], ls[G1][W];
         if (whole) fold_group(std::true_type{}, 0, hs, ls);
@@ -633,8 +703,13 @@ __global__ void __launch_bounds__(TT_THREADS, 1) reduce_tree_rm_kernel(const __g
         rm_tree<G1, W>(hs, ls);
         if constexpr (G2 > 0) {
           f2_t hs2[G2][W], ls2[G2][W];
-          if (whole) fold_group(std::true_type{}, RM_GROUP, hs2, ls2);
-          else fold_group(std::false_type{}, RM_GROUP, hs2, ls2);
+          if constexpr (PK > 1) {
+            if (whole) fold_packed(std::true_type{}, hs2, ls2);
+            else fold_packed(std::false_type{}, hs2, ls2);
+          } else {
+            if (whole) fold_group(std::true_type{}, RM_GROUP, hs2, ls2);
+            else fold_group(std::false_type{}, RM_GROUP, hs2, ls2);
+          }
           rm_tree<G2, W>(hs2, ls2);
           rm_merge<W>(hs[0], ls[0], hs2[0], ls2[0]);
         }
