@@ -147,6 +147,16 @@ def test_fullsize_gpt2_small_single_pass_tree_order(dev):
                  mode=dp.DP_SUM_COMPENSATED | dp.DP_ORDER_TREE)
 
 
+def test_fullsize_gpt_1p3b_tree_order(dev):
+    """The 1.3B list's +3-misaligned 25M-bucket ZeRO-3 layout, warm m/v, with the tree order's two-pass step."""
+    run_fullsize(synth.WORKLOADS["gpt_1p3b"], warm=True, mode=dp.DP_SUM_COMPENSATED | dp.DP_ORDER_TREE)
+
+
+def test_fullsize_llama7b_16l_single_pass_tree_order(dev):
+    """The Llama-16L list (n = 4, a = 2, outliers, loss scale 1) through the tree order's single pass."""
+    run_fullsize(synth.WORKLOADS["llama7b_16l"], single=True, mode=dp.DP_SUM_COMPENSATED | dp.DP_ORDER_TREE)
+
+
 def test_fullsize_gpt_1p3b_single_pass(dev):
     """The 1.3B list's +3-misaligned 25M-bucket ZeRO-3 layout through the single pass, warm m/v."""
     run_fullsize(synth.WORKLOADS["gpt_1p3b"], warm=True, single=True)
